@@ -1,0 +1,175 @@
+"""ctypes binding of libgdn (include/gdn.h): argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; this module
+checks dtypes/devices/shapes of torch tensors, passes raw device pointers and
+the current CUDA stream, and turns status codes into exceptions.  It never
+falls back to another implementation: if the library is missing, loading
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libgdn.so")
+_lock = threading.Lock()
+_lib = None
+
+GDN_OK = 0
+STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED",
+                3: "GDN_ERR_ALIGNMENT", 4: "GDN_ERR_CUDA", 5: "GDN_ERR_DEVICE_STATUS",
+                6: "GDN_ERR_WORKSPACE"}
+EXPORTED = ("gdn_status_string", "gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_decode",
+            "gdn_check_device_status")
+
+
+class GdnError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(msg)
+        self.code = code
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("total_tokens", ctypes.c_int32),
+                ("hq", ctypes.c_int32), ("hk", ctypes.c_int32), ("hv", ctypes.c_int32),
+                ("dk", ctypes.c_int32), ("dv", ctypes.c_int32)]
+
+
+def load(path: Optional[str] = None):
+    """Load libgdn.so (built by ``build.build()``); raises if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise ImportError(
+                    f"libgdn.so not found at {p}: build it with "
+                    "gated_deltanet_linear_08_gb300.build.build() (needs nvcc)")
+            lib = ctypes.CDLL(p)
+            P, f32, sz = ctypes.c_void_p, ctypes.c_float, ctypes.c_size_t
+            lib.gdn_status_string.argtypes = [ctypes.c_int]
+            lib.gdn_status_string.restype = ctypes.c_char_p
+            lib.gdn_prefill_workspace_bytes.argtypes = [ctypes.POINTER(Shape)]
+            lib.gdn_prefill_workspace_bytes.restype = sz
+            lib.gdn_prefill.argtypes = [ctypes.POINTER(Shape), P, P, P, P, P, P, P, P, P, P, P,
+                                        f32, P, P, P, sz, P]
+            lib.gdn_prefill.restype = ctypes.c_int
+            lib.gdn_decode.argtypes = [ctypes.POINTER(Shape), P, P, P, P, P, P, P, P, P, P, f32,
+                                       P, P]
+            lib.gdn_decode.restype = ctypes.c_int
+            lib.gdn_check_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+            lib.gdn_check_device_status.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return load().gdn_status_string(int(code)).decode()
+
+
+def _check(code: int):
+    if code != GDN_OK:
+        raise GdnError(code, status_string(code))
+
+
+def make_shape(num_seqs: int, total_tokens: int, hk: int, hv: int, hq: Optional[int] = None,
+               dk: int = 128, dv: int = 128) -> Shape:
+    return Shape(num_seqs, total_tokens, hk if hq is None else hq, hk, hv, dk, dv)
+
+
+def workspace_bytes(num_seqs: int, total_tokens: int, hk: int, hv: int) -> int:
+    s = make_shape(num_seqs, total_tokens, hk, hv)
+    return int(load().gdn_prefill_workspace_bytes(ctypes.byref(s)))
+
+
+def _ptr(t: Optional[torch.Tensor], dtype, name: str, device) -> Optional[int]:
+    if t is None:
+        return None
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name}: expected device {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    return t.data_ptr()
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream], device) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def alloc_workspace(num_seqs: int, total_tokens: int, hk: int, hv: int, device) -> torch.Tensor:
+    """Device workspace for gdn_prefill (torch allocation, 1024-byte aligned)."""
+    n = workspace_bytes(num_seqs, total_tokens, hk, hv)
+    buf = torch.empty(n + 1024, dtype=torch.uint8, device=device)
+    off = (-buf.data_ptr()) % 1024
+    return buf[off:off + n] if n else buf[:0]
+
+
+def prefill(q, k, v, a, b, A_log, dt_bias, cu_seqlens, init_state=None, z=None, norm_w=None,
+            eps: float = 1e-6, out=None, final_state=None, workspace=None, stream=None):
+    """Chunked GDN prefill through ``gdn_prefill``.  Returns (out, final_state).
+
+    q, k [T, Hk, 128] bf16; v [T, Hv, 128] bf16; a, b [T, Hv] bf16; A_log,
+    dt_bias [Hv] fp32; cu_seqlens [N+1] int32 (device); init_state
+    [N, Hv, 128, 128] fp32 or None; z [T, Hv, 128] bf16 and norm_w [128] bf16
+    for the gated-RMSNorm epilogue.  ``final_state`` may be ``init_state``.
+    """
+    dev = q.device
+    T, hk = q.shape[0], q.shape[1]
+    hv = v.shape[1]
+    N = cu_seqlens.shape[0] - 1
+    if out is None:
+        out = torch.empty(T, hv, 128, dtype=torch.bfloat16, device=dev)
+    if final_state is None:
+        final_state = torch.empty(N, hv, 128, 128, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(N, T, hk, hv, dev)
+    bf, f32 = torch.bfloat16, torch.float32
+    shape = make_shape(N, T, hk, hv)
+    code = load().gdn_prefill(
+        ctypes.byref(shape), _ptr(q, bf, "q", dev), _ptr(k, bf, "k", dev), _ptr(v, bf, "v", dev),
+        _ptr(a, bf, "a", dev), _ptr(b, bf, "b", dev), _ptr(A_log, f32, "A_log", dev),
+        _ptr(dt_bias, f32, "dt_bias", dev), _ptr(init_state, f32, "init_state", dev),
+        _ptr(cu_seqlens, torch.int32, "cu_seqlens", dev), _ptr(z, bf, "z", dev),
+        _ptr(norm_w, bf, "norm_w", dev), float(eps), _ptr(out, bf, "out", dev),
+        _ptr(final_state, f32, "final_state", dev), _ptr(workspace, torch.uint8, "workspace", dev),
+        int(workspace.numel()), _stream_handle(stream, dev))
+    _check(code)
+    return out, final_state
+
+
+def decode(q, k, v, a, b, A_log, dt_bias, state, z=None, norm_w=None, eps: float = 1e-6,
+           out=None, stream=None):
+    """One decode token per sequence through ``gdn_decode``; ``state`` is
+    updated in place.  Returns out [B, Hv, 128] bf16."""
+    dev = q.device
+    B, hk = q.shape[0], q.shape[1]
+    hv = v.shape[1]
+    if out is None:
+        out = torch.empty(B, hv, 128, dtype=torch.bfloat16, device=dev)
+    bf, f32 = torch.bfloat16, torch.float32
+    shape = make_shape(B, B, hk, hv)
+    code = load().gdn_decode(
+        ctypes.byref(shape), _ptr(q, bf, "q", dev), _ptr(k, bf, "k", dev), _ptr(v, bf, "v", dev),
+        _ptr(a, bf, "a", dev), _ptr(b, bf, "b", dev), _ptr(A_log, f32, "A_log", dev),
+        _ptr(dt_bias, f32, "dt_bias", dev), _ptr(state, f32, "state", dev),
+        _ptr(z, bf, "z", dev), _ptr(norm_w, bf, "norm_w", dev), float(eps),
+        _ptr(out, bf, "out", dev), _stream_handle(stream, dev))
+    _check(code)
+    return out
+
+
+def check_device_status() -> int:
+    """Synchronise and read/clear the kernels' status bits (0 = clean)."""
+    bits = ctypes.c_uint32(0)
+    code = load().gdn_check_device_status(ctypes.byref(bits))
+    if code not in (GDN_OK, 5):
+        _check(code)
+    return int(bits.value)

@@ -1,0 +1,175 @@
+// gdn_decode.cu -- single-token GDN decode with the fp32 state updated in
+// place (the per-request recurrent-state slots of serving: SGLang page
+// "[Perf] Pack the Qwen3.5 GDN input projection on CUDA", Accuracy Tests,
+// "16 mamba slots").
+//
+// One CTA per (sequence, value head) streams its 128x128 fp32 state (64 KB)
+// exactly once: every thread keeps 16 rows x 4 columns of the state in
+// registers between the read and the write.  The update needs
+//   r_k = S_old^T kn,  r_q = S_old^T qn          (reductions over Dk)
+//   delta = beta (v - e^g r_k)
+//   o = scale (e^g r_q + (kn . qn) delta)        (= scale * S_new^T qn)
+//   S_new = e^g S_old + kn delta^T
+// so both reductions come from the old state in the same pass and the write
+// follows once delta is known.  The path is HBM-bound (about 7 flop per 8
+// bytes of state): loads and stores are 16-byte, warp-contiguous rows of 512
+// bytes, marked streaming so they do not displace other data in L2.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kRowsPerThread = kD / kWarps;  // 16
+
+template <bool kNorm>
+__global__ void __launch_bounds__(kThreads, 2)
+decode_kernel(DecodeArgs p)
+{
+    const int h = blockIdx.x, n = blockIdx.y;
+    const int hv = p.hv, hk = p.hk;
+    const int hq = h / (hv / hk);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    __shared__ float s_k[kD], s_q[kD], s_v[kD], s_delta[kD];
+    __shared__ float s_part[2][kWarps][kD];
+    __shared__ float s_scal[4];   // e^g, beta, kn.qn
+    __shared__ float s_red[4];
+
+    float *S = p.state + ((size_t)n * hv + h) * (size_t)(kD * kD);
+
+    // 1. Issue every state load first so the whole 64 KB is in flight.
+    float4 st[kRowsPerThread];
+#pragma unroll
+    for (int i = 0; i < kRowsPerThread; ++i)
+        st[i] = __ldcs(reinterpret_cast<const float4 *>(S + (size_t)(warp + kWarps * i) * kD) + lane);
+
+    // 2. Per-token inputs: warp 0 normalises k, warp 1 q, warp 2 loads v,
+    //    warp 3 computes the gate and beta.
+    if (warp < 2) {
+        const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(warp == 0 ? p.k : p.q)
+                                   + ((size_t)n * hk + hq) * kD + lane * 4;
+        const uint2 u = *reinterpret_cast<const uint2 *>(src);
+        float f[4] = {__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                      __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u)};
+        float ss = f[0] * f[0] + f[1] * f[1] + f[2] * f[2] + f[3] * f[3];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float r = 1.f / sqrtf(ss + kL2Eps);
+        float *dst = warp == 0 ? s_k : s_q;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            dst[lane * 4 + j] = f[j] * r;
+    } else if (warp == 2) {
+        const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(p.v)
+                                   + ((size_t)n * hv + h) * kD + lane * 4;
+        const uint2 u = *reinterpret_cast<const uint2 *>(src);
+        s_v[lane * 4 + 0] = __uint_as_float(u.x << 16);
+        s_v[lane * 4 + 1] = __uint_as_float(u.x & 0xFFFF0000u);
+        s_v[lane * 4 + 2] = __uint_as_float(u.y << 16);
+        s_v[lane * 4 + 3] = __uint_as_float(u.y & 0xFFFF0000u);
+    } else if (warp == 3 && lane == 0) {
+        const float av = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.a)[(size_t)n * hv + h]);
+        const float bv = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.b)[(size_t)n * hv + h]);
+        s_scal[0] = expf(gate_f(av, p.A_log[h], p.dt_bias[h]));
+        s_scal[1] = sigmoid_f(bv);
+    }
+    __syncthreads();
+
+    // 3. Partial reductions over this thread's 16 rows, for 4 columns.
+    float rk[4] = {0.f, 0.f, 0.f, 0.f}, rq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < kRowsPerThread; ++i) {
+        const int r = warp + kWarps * i;
+        const float kk = s_k[r], qq = s_q[r];
+        rk[0] = fmaf(st[i].x, kk, rk[0]); rq[0] = fmaf(st[i].x, qq, rq[0]);
+        rk[1] = fmaf(st[i].y, kk, rk[1]); rq[1] = fmaf(st[i].y, qq, rq[1]);
+        rk[2] = fmaf(st[i].z, kk, rk[2]); rq[2] = fmaf(st[i].z, qq, rq[2]);
+        rk[3] = fmaf(st[i].w, kk, rk[3]); rq[3] = fmaf(st[i].w, qq, rq[3]);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        s_part[0][warp][lane * 4 + j] = rk[j];
+        s_part[1][warp][lane * 4 + j] = rq[j];
+    }
+    if (warp == 0) {
+        float kq = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            kq = fmaf(s_k[lane * 4 + j], s_q[lane * 4 + j], kq);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            kq += __shfl_xor_sync(0xffffffffu, kq, o);
+        if (lane == 0)
+            s_scal[2] = kq;
+    }
+    __syncthreads();
+
+    // 4. Column c = tid (< 128): delta and the output.
+    const float eg = s_scal[0], beta = s_scal[1];
+    const float scale = rsqrtf((float)kD);
+    float o = 0.f;
+    if (tid < kD) {
+        float sk = 0.f, sq = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            sk += s_part[0][w][tid];
+            sq += s_part[1][w][tid];
+        }
+        const float delta = beta * (s_v[tid] - eg * sk);
+        s_delta[tid] = delta;
+        o = scale * (eg * sq + s_scal[2] * delta);
+        if (kNorm) {
+            float ss = o * o;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            if (lane == 0)
+                s_red[warp] = ss;
+        }
+    }
+    __syncthreads();
+    if (tid < kD) {
+        __nv_bfloat16 *outp = reinterpret_cast<__nv_bfloat16 *>(p.out) + ((size_t)n * hv + h) * kD;
+        if (kNorm) {
+            const float ms = (s_red[0] + s_red[1] + s_red[2] + s_red[3]) * (1.f / kD);
+            const float zz = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.z)[((size_t)n * hv + h) * kD + tid]);
+            const float ww = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.norm_w)[tid]);
+            o = o * rsqrtf(ms + p.eps) * ww * (zz * sigmoid_f(zz));
+        }
+        outp[tid] = __float2bfloat16_rn(o);
+    }
+
+    // 5. S_new = e^g S_old + kn delta^T, written back in place.
+    const float4 d4 = *reinterpret_cast<const float4 *>(&s_delta[lane * 4]);
+#pragma unroll
+    for (int i = 0; i < kRowsPerThread; ++i) {
+        const int r = warp + kWarps * i;
+        const float kk = s_k[r];
+        float4 x = st[i];
+        x.x = fmaf(eg, x.x, kk * d4.x);
+        x.y = fmaf(eg, x.y, kk * d4.y);
+        x.z = fmaf(eg, x.z, kk * d4.z);
+        x.w = fmaf(eg, x.w, kk * d4.w);
+        __stcs(reinterpret_cast<float4 *>(S + (size_t)r * kD) + lane, x);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs &args, cudaStream_t stream)
+{
+    if (args.batch == 0)
+        return cudaSuccess;
+    dim3 grid(args.hv, args.batch);
+    if (args.z)
+        decode_kernel<true><<<grid, kThreads, 0, stream>>>(args);
+    else
+        decode_kernel<false><<<grid, kThreads, 0, stream>>>(args);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

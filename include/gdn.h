@@ -1,0 +1,135 @@
+/*
+ * gdn.h -- C ABI of libgdn, the Gated DeltaNet (GDN) linear-attention layer
+ * core for NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes.  Per token t of sequence n and value head h
+ * (key/query head hk = h / (Hv/Hk), contiguous groups of value heads):
+ *     g_t    = -exp(A_log[h]) * softplus(a[t,h] + dt_bias[h])
+ *     beta_t = sigmoid(b[t,h])
+ *     qn_t   = q[t,hk] / sqrt(sum q^2 + 1e-6),  kn_t likewise
+ *     S_t    = exp(g_t) S_{t-1} + kn_t (beta_t (v_t - exp(g_t) S_{t-1}^T kn_t))^T
+ *     o_t    = S_t^T qn_t / sqrt(Dk)
+ * with the fp32 state S held as Dk x Dv per (sequence, value head).  These are
+ * the ingredients the JevAny page lists for the chunked GDN kernel ("Add
+ * opt-in fused Qwen3.5 inference kernels", section Summary: gate from A_log
+ * and dt_bias, beta sigmoid, q/k L2 norm, grouped value heads, followed by a
+ * fused gated RMSNorm); the state layout is the "HKV" layout of the pegainfer
+ * page ("feat(qwen35): add SM120 FlashInfer GDN prefill candidate", sections
+ * Summary and Correctness).  Optional epilogue (JevAny page, Summary):
+ *     y_t = o_t / sqrt(mean(o_t^2) + eps) * w * silu(z_t)   over Dv, per head.
+ *
+ * Boundary conventions (pegainfer page, review: a stable C ABI that owns the
+ * kernel, unsupported shapes handled explicitly):
+ *   - Every pointer is a DEVICE pointer unless stated otherwise.  The caller
+ *     owns every buffer and the stream; the library never allocates, frees,
+ *     prints, aborts or traps, and issues no host<->device synchronisation in
+ *     gdn_prefill / gdn_decode.
+ *   - Layouts are row-major, innermost index last, densely packed.
+ *   - bf16 tensors and fp32 state/workspace pointers must be 16-byte aligned
+ *     (GDN_ERR_ALIGNMENT otherwise); the workspace must be 1024-byte aligned.
+ *   - Only Dk = Dv = 128, Hq == Hk and Hv % Hk == 0 are supported; anything
+ *     else returns GDN_ERR_UNSUPPORTED before any launch.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  A launch failure returns GDN_ERR_CUDA.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct {
+    int32_t num_seqs;     /* N: packed sequences (prefill) or batch (decode) */
+    int32_t total_tokens; /* T_tot = cu_seqlens[N] (prefill); == N for decode */
+    int32_t hq, hk, hv;   /* query, key and value heads; hq == hk, hv % hk == 0 */
+    int32_t dk, dv;       /* head dims; both must be 128 */
+} gdn_shape_t;
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,    /* null required pointer, negative size, aliasing */
+    GDN_ERR_UNSUPPORTED = 2,    /* shape outside Dk=Dv=128, Hq==Hk, Hv%Hk==0 */
+    GDN_ERR_ALIGNMENT = 3,      /* pointer not 16-byte (workspace: 1024-byte) aligned */
+    GDN_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed */
+    GDN_ERR_DEVICE_STATUS = 5,  /* a kernel recorded an error (bounded wait ran out) */
+    GDN_ERR_WORKSPACE = 6       /* workspace NULL or smaller than required */
+} gdn_status_t;
+
+/* Human-readable name of a status code; never NULL. */
+const char *gdn_status_string(gdn_status_t status);
+
+/* Bytes of device workspace gdn_prefill needs for this shape (0 for an empty
+ * problem).  Depends only on num_seqs, total_tokens, hk and hv.  Host-only. */
+size_t gdn_prefill_workspace_bytes(const gdn_shape_t *shape);
+
+/*
+ * gdn_prefill -- chunked (64-token) prefill over packed variable-length
+ * sequences (pegainfer page, Correctness: chunked vs unchunked prefill,
+ * T = 1, 2, 63, 64, 65, 127, 128 operator boundaries; varlen packing).
+ *
+ *   q, k        bf16 [T_tot, Hk, 128]
+ *   v           bf16 [T_tot, Hv, 128]
+ *   a, b        bf16 [T_tot, Hv]
+ *   A_log       fp32 [Hv]
+ *   dt_bias     fp32 [Hv]
+ *   init_state  fp32 [N, Hv, 128(k), 128(v)], or NULL for zero initial states
+ *   cu_seqlens  int32 [N+1] on the device: cu[0] = 0, non-decreasing,
+ *               cu[N] = T_tot.  Empty sequences are allowed (their final
+ *               state is their initial state).  Not read on the host.
+ *   z           bf16 [T_tot, Hv, 128] or NULL; NULL disables the epilogue
+ *   norm_w      bf16 [128] (required when z != NULL), eps its epsilon
+ *   out         bf16 [T_tot, Hv, 128]; must not overlap any input
+ *   final_state fp32 [N, Hv, 128, 128]; may equal init_state (in place)
+ *   workspace   device scratch of at least gdn_prefill_workspace_bytes(shape)
+ *               bytes, 1024-byte aligned, owned by the caller; its contents
+ *               need no initialisation and are garbage afterwards.  Calls that
+ *               share one workspace must be ordered on the GPU.
+ * Returns GDN_OK once the work is enqueued.
+ */
+gdn_status_t gdn_prefill(const gdn_shape_t *shape,
+                         const void *q, const void *k, const void *v,
+                         const void *a, const void *b,
+                         const float *A_log, const float *dt_bias,
+                         const float *init_state, const int32_t *cu_seqlens,
+                         const void *z, const void *norm_w, float eps,
+                         void *out, float *final_state,
+                         void *workspace, size_t workspace_bytes,
+                         void *stream);
+
+/*
+ * gdn_decode -- one token per sequence, the state updated in place (the
+ * recurrent-state slots of serving, SGLang page "[Perf] Pack the Qwen3.5 GDN
+ * input projection on CUDA", section Accuracy Tests: mamba slots).  Each
+ * 128x128 fp32 state is read once and written once.
+ *
+ *   shape->total_tokens must equal shape->num_seqs (= batch B).
+ *   q, k   bf16 [B, Hk, 128];  v bf16 [B, Hv, 128];  a, b bf16 [B, Hv]
+ *   A_log, dt_bias fp32 [Hv]
+ *   state  fp32 [B, Hv, 128, 128], read and overwritten in place
+ *   z      bf16 [B, Hv, 128] or NULL (no epilogue); norm_w bf16 [128]; eps
+ *   out    bf16 [B, Hv, 128]; must not overlap any input or the state
+ * Needs no workspace.
+ */
+gdn_status_t gdn_decode(const gdn_shape_t *shape,
+                        const void *q, const void *k, const void *v,
+                        const void *a, const void *b,
+                        const float *A_log, const float *dt_bias,
+                        float *state,
+                        const void *z, const void *norm_w, float eps,
+                        void *out, void *stream);
+
+/* Reads and clears the device status word that kernels set when a bounded
+ * wait runs out.  Synchronises the device: not for the hot path.  Returns
+ * GDN_OK, GDN_ERR_DEVICE_STATUS (and the raw bits in *bits when non-NULL),
+ * or GDN_ERR_CUDA. */
+gdn_status_t gdn_check_device_status(uint32_t *bits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

@@ -1,0 +1,119 @@
+"""Host-side checks of the C ABI (no GPU): the library builds and loads, exports
+every function include/gdn.h declares, and rejects bad arguments with the
+documented status codes before any CUDA call (pegainfer page, maintainer
+review: a stable C ABI, unsupported shapes handled explicitly).
+
+The pointers passed here are fake integers; every case returns during host
+validation, before anything could dereference them or touch a device.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gated_deltanet_linear_08_gb300 import _binding as B
+from gated_deltanet_linear_08_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return B.load()
+
+
+def _declared_functions():
+    with open(os.path.join(ROOT, "include", "gdn.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert set(names) == set(B.EXPORTED), names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code, name in B.STATUS_NAMES.items():
+        assert B.status_string(code).startswith(name)
+    assert B.status_string(99) == "GDN_ERR_UNKNOWN"
+
+
+def test_workspace_bytes_formula(lib):
+    # per (chunk, v head) 65 KiB, per (chunk, k head) 16 KiB; chunks <= ceil(T/64) + N
+    assert B.workspace_bytes(1, 2048, 16, 32) == (32 + 1) * (32 * 66560 + 16 * 16384)
+    assert B.workspace_bytes(8, 1024, 16, 32) == (16 + 8) * (32 * 66560 + 16 * 16384)
+    assert B.workspace_bytes(3, 0, 16, 32) == 0
+    s = B.make_shape(1, 64, 16, 32, dk=64)
+    assert lib.gdn_prefill_workspace_bytes(ctypes.byref(s)) == 0   # unsupported -> 0
+
+
+FAKE = 0x7f0000000000   # 1024-byte aligned, never dereferenced
+
+
+def _prefill(lib, shape, **kw):
+    args = dict(q=FAKE, k=FAKE + 0x10000000, v=FAKE + 0x20000000, a=FAKE + 0x30000000,
+                b=FAKE + 0x40000000, A_log=FAKE + 0x50000000, dt_bias=FAKE + 0x60000000,
+                init=None, cu=FAKE + 0x70000000, z=None, w=None, eps=1e-6,
+                out=FAKE + 0x80000000, fin=FAKE + 0x90000000, ws=FAKE + 0xA0000000,
+                ws_bytes=1 << 40)
+    args.update(kw)
+    return lib.gdn_prefill(ctypes.byref(shape) if shape is not None else None, args["q"],
+                           args["k"], args["v"], args["a"], args["b"], args["A_log"],
+                           args["dt_bias"], args["init"], args["cu"], args["z"], args["w"],
+                           args["eps"], args["out"], args["fin"], args["ws"], args["ws_bytes"],
+                           None)
+
+
+def test_prefill_rejects_bad_arguments(lib):
+    ok = B.make_shape(1, 64, 16, 32)
+    assert _prefill(lib, None) == 1
+    assert _prefill(lib, B.make_shape(1, 64, 16, 32, dk=64)) == 2
+    assert _prefill(lib, B.make_shape(1, 64, 16, 32, dv=256)) == 2
+    assert _prefill(lib, B.make_shape(1, 64, 16, 32, hq=32)) == 2
+    assert _prefill(lib, B.make_shape(1, 64, 16, 40)) == 2
+    assert _prefill(lib, B.make_shape(-1, 64, 16, 32)) == 1
+    assert _prefill(lib, ok, q=None) == 1
+    assert _prefill(lib, ok, cu=None) == 1
+    assert _prefill(lib, ok, z=FAKE + 0xB0000000) == 1          # z without norm_w
+    assert _prefill(lib, ok, eps=-1.0) == 1
+    assert _prefill(lib, ok, q=FAKE + 8) == 3                   # misaligned bf16 tensor
+    assert _prefill(lib, ok, ws=FAKE + 0xA0000000 + 512) == 3   # workspace not 1024-aligned
+    assert _prefill(lib, ok, ws=None) == 6
+    assert _prefill(lib, ok, ws_bytes=1000) == 6
+    assert _prefill(lib, ok, out=FAKE + 0x100) == 1             # out overlaps q
+    assert _prefill(lib, ok, init=FAKE + 0x90000000 + 4096) == 1  # partial state overlap
+    assert _prefill(lib, B.make_shape(0, 5, 16, 32)) == 1       # tokens without sequences
+    assert _prefill(lib, B.make_shape(0, 0, 16, 32)) == 0       # empty problem: no-op
+
+
+def test_decode_rejects_bad_arguments(lib):
+    def dec(shape, **kw):
+        a = dict(q=FAKE, k=FAKE + 0x10000000, v=FAKE + 0x20000000, a=FAKE + 0x30000000,
+                 b=FAKE + 0x40000000, A_log=FAKE + 0x50000000, dt=FAKE + 0x60000000,
+                 state=FAKE + 0x70000000, z=None, w=None, eps=1e-6, out=FAKE + 0x90000000)
+        a.update(kw)
+        return lib.gdn_decode(ctypes.byref(shape), a["q"], a["k"], a["v"], a["a"], a["b"],
+                              a["A_log"], a["dt"], a["state"], a["z"], a["w"], a["eps"],
+                              a["out"], None)
+    assert dec(B.make_shape(4, 5, 16, 32)) == 1                 # total_tokens != batch
+    assert dec(B.make_shape(4, 4, 16, 32, dk=96)) == 2
+    assert dec(B.make_shape(4, 4, 16, 32), state=None) == 1
+    assert dec(B.make_shape(4, 4, 16, 32), v=FAKE + 0x20000000 + 2) == 3
+    assert dec(B.make_shape(4, 4, 16, 32), out=FAKE + 0x70000000) == 1   # out overlaps state
+    assert dec(B.make_shape(0, 0, 16, 32)) == 0
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    saved = B._lib
+    try:
+        B._lib = None
+        with pytest.raises(ImportError):
+            B.load(str(tmp_path / "nope.so"))
+    finally:
+        B._lib = saved

@@ -1,0 +1,115 @@
+"""GPU parity of gdn_prefill against the fp64 oracle.
+
+Covers the four prefill workloads (T=64; 8x128 packed with initial states;
+T=2048 with the gated-RMSNorm epilogue, also as 2x1024 with the state
+carried; 16 varlen sequences at Hv=48), the chunk boundaries the pegainfer
+page tests ("feat(qwen35): add SM120 FlashInfer GDN prefill candidate",
+Correctness: T = 1, 2, 63, 64, 65, 127, 128; chunked vs unchunked prefill),
+grouped heads, empty sequences, in-place state, weak and pure decay, and
+run-to-run determinism.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from gated_deltanet_linear_08_gb300.inputs import (CASE_8x128, CASE_T64, CASE_T2048,
+                                                   CASE_VARLEN48, PrefillCase,
+                                                   make_prefill_inputs)
+from parity_util import (assert_out_close, assert_state_close, gpu_prefill, oracle_prefill,
+                         out_stats, state_stats)
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(case, in_place=False, scale_state=False):
+    x = make_prefill_inputs(case)
+    ro, rs = oracle_prefill(x)
+    go, gs = gpu_prefill(x, in_place=in_place)
+    so = assert_out_close(go, ro, case.name + " out")
+    ss = assert_state_close(gs, rs, case.name + " state", scale_with_ref=scale_state)
+    print(case.name, "out", so, "state", ss)
+    return x, go, gs
+
+
+@pytest.mark.parametrize("case", [CASE_T64, CASE_8x128, CASE_T2048, CASE_VARLEN48],
+                         ids=lambda c: c.name)
+def test_prefill_workloads(case):
+    _check(case)
+
+
+@pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 127, 128])
+def test_prefill_chunk_boundaries(T):
+    _check(PrefillCase(f"T{T}", seqlens=[T], init_state=True, seed=T))
+
+
+def test_prefill_grouped_heads_ratio3_and_ragged():
+    _check(PrefillCase("g3", seqlens=[70, 1, 130, 64], hk=2, hv=6, init_state=True, seed=3))
+
+
+def test_prefill_empty_sequences():
+    x, go, gs = _check(PrefillCase("empty", seqlens=[0, 5, 0, 64, 0], hk=2, hv=4,
+                                   init_state=True, seed=4))
+    init = x["init_state"].double().numpy()
+    for n in (0, 2, 4):
+        assert np.array_equal(gs[n], init[n])
+
+
+def test_prefill_in_place_state():
+    _check(PrefillCase("inplace", seqlens=[100, 28], hk=2, hv=4, init_state=True, seed=5),
+           in_place=True)
+
+
+def test_prefill_weak_decay_carries_state():
+    _check(PrefillCase("weak", seqlens=[700], hk=2, hv=4, init_state=True, seed=6,
+                       a_log_const=math.log(0.01)), scale_state=True)
+
+
+def test_prefill_pure_decay():
+    """b -> -inf gives beta = 0: the state only decays (e^{sum g} S0)."""
+    _check(PrefillCase("decay", seqlens=[150], hk=2, hv=4, init_state=True, seed=7,
+                       a_log_const=math.log(0.02), b_const=-1e4))
+
+
+def test_prefill_gated_norm_small():
+    _check(PrefillCase("gn", seqlens=[65, 130], hk=2, hv=4, init_state=True, gated_norm=True,
+                       seed=8))
+
+
+@pytest.mark.parametrize("gated", [False, True])
+def test_prefill_2x1024_carried_state_matches_single_call(gated):
+    """T=2048 in one call vs two 1024-token calls with the state carried: chunk
+    boundaries coincide, so the results are bitwise equal."""
+    import gated_deltanet_linear_08_gb300 as gdn
+    x = make_prefill_inputs(PrefillCase("c", seqlens=[2048], gated_norm=gated, init_state=True,
+                                        seed=9))
+    dev = "cuda"
+    d = {k: (None if x[k] is None else x[k].to(dev)) for k in
+         ("q", "k", "v", "a", "b", "A_log", "dt_bias", "init_state", "z", "norm_w")}
+    cu = x["cu_seqlens"].to(dev)
+    out1, fin1 = gdn.prefill(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], cu,
+                             init_state=d["init_state"], z=d["z"], norm_w=d["norm_w"], eps=x["eps"])
+    half = torch.tensor([0, 1024], dtype=torch.int32, device=dev)
+    sl = lambda t, lo, hi: None if t is None else t[lo:hi].contiguous()
+    oa, fa = gdn.prefill(sl(d["q"], 0, 1024), sl(d["k"], 0, 1024), sl(d["v"], 0, 1024),
+                         sl(d["a"], 0, 1024), sl(d["b"], 0, 1024), d["A_log"], d["dt_bias"], half,
+                         init_state=d["init_state"], z=sl(d["z"], 0, 1024), norm_w=d["norm_w"],
+                         eps=x["eps"])
+    ob, fb = gdn.prefill(sl(d["q"], 1024, 2048), sl(d["k"], 1024, 2048), sl(d["v"], 1024, 2048),
+                         sl(d["a"], 1024, 2048), sl(d["b"], 1024, 2048), d["A_log"], d["dt_bias"],
+                         half, init_state=fa, z=sl(d["z"], 1024, 2048), norm_w=d["norm_w"],
+                         eps=x["eps"])
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat([oa, ob]), out1)
+    assert torch.equal(fb, fin1)
+
+
+def test_prefill_deterministic_and_stream():
+    x = make_prefill_inputs(PrefillCase("det", seqlens=[300, 17], hk=2, hv=4, init_state=True,
+                                        gated_norm=True, seed=10))
+    o1, s1 = gpu_prefill(x)
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        o2, s2 = gpu_prefill(x, stream=st)
+    assert np.array_equal(o1, o2) and np.array_equal(s1, s2)
