@@ -1,0 +1,463 @@
+#!/usr/bin/env python3
+"""Benchmark of the GDN layer core on GB300: prefill tokens/s and decode GB/s.
+
+One step = one pass of the whole path on synthetic inputs of the pages'
+Qwen3.5-4B geometry (Hq/Hk/Hv/D = 16/16/32/128):
+  * gdn_prefill over one T=2048 sequence with the gated-RMSNorm epilogue
+    (prep kernel + scan kernel), inputs rotated over 8 buffer sets so every
+    step reads them from HBM (8 sets x ~67 MB of inputs >> 126 MB of L2);
+  * gdn_decode of one token for 256 sequences, the 512 MiB fp32 state updated
+    in place (larger than L2 by itself).
+`value` is prefill tokens/s; the decode figures sit in the "decode" object.
+CUDA events bracket each call inside the timed region, so each kernel family
+gets its own measured time; the step time is the whole region / K.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+N > 1 runs under torchrun: each rank processes its own replica (no data-path
+collective), the timing is the max over ranks and `value` sums all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gated_deltanet_linear_08_gb300.inputs import (CASE_DECODE, CASE_T2048, DecodeCase,  # noqa: E402
+                                                   PrefillCase, make_decode_inputs,
+                                                   make_prefill_inputs)
+
+METRIC = "GDN prefill tokens/s & decode GB/s at Hv=32,D=128; % of tensor/HBM roofline"
+PREFILL_FLOP_PER_TOKEN_HEAD = 10 * 64 * 128 + 6 * 128 * 128   # 180,224 (C=64 chunked count)
+N_ROTATE = 8
+KERNEL_SOURCES = ["gdn_api.cu", "gdn_decode.cu", "gdn_prefill_prep.cu", "gdn_prefill_scan.cu",
+                  "common.cuh", "tc05.cuh", "kernels.h"]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "gated_deltanet_linear_08_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kind: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    return d.get(kind)
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+def build_prefill_sets(dev, case: PrefillCase, n_sets: int):
+    import gated_deltanet_linear_08_gb300 as gdn
+    x = make_prefill_inputs(case)
+    T, hk, hv, N = x["q"].shape[0], case.hk, case.hv, len(x["seqlens"])
+    shared = {k: x[k].to(dev) for k in ("A_log", "dt_bias", "cu_seqlens", "norm_w")}
+    sets = []
+    for _ in range(n_sets):
+        s = {k: x[k].to(dev) for k in ("q", "k", "v", "a", "b", "z")}
+        s["out"] = torch.empty(T, hv, 128, dtype=torch.bfloat16, device=dev)
+        s["fin"] = torch.empty(N, hv, 128, 128, dtype=torch.float32, device=dev)
+        s["ws"] = gdn.alloc_workspace(N, T, hk, hv, dev)
+        sets.append(s)
+    return x, shared, sets
+
+
+def run_prefill(gdn, shared, s, eps, stream):
+    gdn.prefill(s["q"], s["k"], s["v"], s["a"], s["b"], shared["A_log"], shared["dt_bias"],
+                shared["cu_seqlens"], init_state=None, z=s["z"], norm_w=shared["norm_w"],
+                eps=eps, out=s["out"], final_state=s["fin"], workspace=s["ws"], stream=stream)
+
+
+def build_decode(dev, case: DecodeCase):
+    y = make_decode_inputs(DecodeCase(case.name, batch=case.batch, hk=case.hk, hv=case.hv,
+                                      steps=1))
+    d = {k: v.to(dev) for k, v in y["steps"][0].items()}
+    d["A_log"], d["dt_bias"] = y["A_log"].to(dev), y["dt_bias"].to(dev)
+    d["state"] = y["state"].to(dev)
+    d["out"] = torch.empty(case.batch, case.hv, 128, dtype=torch.bfloat16, device=dev)
+    return y, d
+
+
+def run_decode(gdn, d, stream):
+    gdn.decode(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["state"],
+               out=d["out"], stream=stream)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def timed_region(gdn, pre, dec, steps, warmup, stream, world):
+    x, shared, sets = pre
+    eps = x["eps"]
+    for i in range(warmup):
+        run_prefill(gdn, shared, sets[i % len(sets)], eps, stream)
+        run_decode(gdn, dec, stream)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(steps):
+        e = ev[i]
+        e[0].record(stream)
+        run_prefill(gdn, shared, sets[i % len(sets)], eps, stream)
+        e[1].record(stream)
+        e[2].record(stream)
+        run_decode(gdn, dec, stream)
+        e[3].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    total_ms = start.elapsed_time(end)
+    pre_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    dec_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    return total_ms, pre_ms, dec_ms
+
+
+def e2e_region(gdn, x, dec_y, dev, steps, warmup, stream):
+    """Same step through the public API with pinned host buffers: H2D of the
+    step's inputs, both calls, D2H of the results, all inside the timed region."""
+    keys = ("q", "k", "v", "a", "b", "z")
+    h_in = {k: x[k].pin_memory() for k in keys}
+    d_in = {k: torch.empty_like(x[k], device=dev) for k in keys}
+    shared = {k: x[k].to(dev) for k in ("A_log", "dt_bias", "cu_seqlens", "norm_w")}
+    T, hv, N = x["q"].shape[0], x["hv"], len(x["seqlens"])
+    out = torch.empty(T, hv, 128, dtype=torch.bfloat16, device=dev)
+    fin = torch.empty(N, hv, 128, 128, dtype=torch.float32, device=dev)
+    ws = gdn.alloc_workspace(N, T, x["hk"], hv, dev)
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_fin = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+    st = dec_y["steps"][0]
+    dkeys = ("q", "k", "v", "a", "b")
+    hd_in = {k: st[k].pin_memory() for k in dkeys}
+    dd = {k: torch.empty_like(st[k], device=dev) for k in dkeys}
+    dd["A_log"], dd["dt_bias"] = dec_y["A_log"].to(dev), dec_y["dt_bias"].to(dev)
+    dd["state"] = dec_y["state"].to(dev)
+    dd["out"] = torch.empty(st["v"].shape, dtype=torch.bfloat16, device=dev)
+    hd_out = torch.empty(dd["out"].shape, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in list(h_in.values()) + list(hd_in.values()))
+    d2h = (h_out.numel() * 2 + h_fin.numel() * 4 + hd_out.numel() * 2)
+
+    def step():
+        with torch.cuda.stream(stream):
+            for k in keys:
+                d_in[k].copy_(h_in[k], non_blocking=True)
+            gdn.prefill(d_in["q"], d_in["k"], d_in["v"], d_in["a"], d_in["b"], shared["A_log"],
+                        shared["dt_bias"], shared["cu_seqlens"], z=d_in["z"],
+                        norm_w=shared["norm_w"], eps=x["eps"], out=out, final_state=fin,
+                        workspace=ws, stream=stream)
+            h_out.copy_(out, non_blocking=True)
+            h_fin.copy_(fin, non_blocking=True)
+            for k in dkeys:
+                dd[k].copy_(hd_in[k], non_blocking=True)
+            gdn.decode(dd["q"], dd["k"], dd["v"], dd["a"], dd["b"], dd["A_log"], dd["dt_bias"],
+                       dd["state"], out=dd["out"], stream=stream)
+            hd_out.copy_(dd["out"], non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps, h2d, d2h
+
+
+# ---------------------------------------------------------------------------
+# CPU legs: the fp64 oracle as it stands, on the host cores
+# ---------------------------------------------------------------------------
+def _oracle_prefill_sample(T: int):
+    """Oracle prefill on the first T tokens of the T=2048 workload (all 32 heads)."""
+    import oracle
+    from gated_deltanet_linear_08_gb300.inputs import to_f64
+    x = make_prefill_inputs(CASE_T2048)
+    cu = torch.tensor([0, T], dtype=torch.int32).numpy()
+    f = {k: to_f64(x[k]) for k in ("q", "k", "v", "a", "b", "A_log", "dt_bias", "z", "norm_w")}
+    for k in ("q", "k", "v", "a", "b", "z"):
+        f[k] = f[k][:T]
+
+    def run():
+        oracle.prefill(cu, f["q"], f["k"], f["v"], f["a"], f["b"], f["A_log"], f["dt_bias"],
+                       None, f["z"], f["norm_w"], eps=x["eps"], nthreads=os.cpu_count())
+    return run
+
+
+def _oracle_decode_sample(B: int):
+    import numpy as np
+
+    import oracle
+    from gated_deltanet_linear_08_gb300.inputs import to_f64
+    y = make_decode_inputs(DecodeCase("cpu", batch=B, steps=1))
+    st = {k: to_f64(v) for k, v in y["steps"][0].items()}
+    S = np.ascontiguousarray(to_f64(y["state"]))
+    A_log, dt = to_f64(y["A_log"]), to_f64(y["dt_bias"])
+
+    def run():
+        oracle.decode_step(st["q"], st["k"], st["v"], st["a"], st["b"], A_log, dt, S,
+                           nthreads=os.cpu_count())
+    return run
+
+
+def decode_state_bytes(batch: int, hv: int = 32, hk: int = 16) -> int:
+    """Algorithmic bytes of one decode step: every fp32 state read and written
+    once, plus the token inputs and the bf16 output."""
+    state = batch * hv * 128 * 128 * 4 * 2
+    io = batch * (2 * hk * 128 * 2 + hv * 128 * 2 + 2 * hv * 2 + hv * 128 * 2)
+    return state + io
+
+
+def cpu_baseline():
+    pre = _oracle_prefill_sample(2048)
+    t = time.perf_counter(); pre(); tp = time.perf_counter() - t
+    dec = _oracle_decode_sample(16)
+    t = time.perf_counter(); dec(); td = time.perf_counter() - t
+    return {"value": 2048 / tp, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": "fp64 oracle, the full T=2048 prefill (32 heads, gated norm), once; "
+                      "decode: 16 of the 256 sequences, one step",
+            "seconds": round(tp, 3),
+            "decode": {"value": decode_state_bytes(16) / td / 1e9, "unit": "GB/s",
+                       "tokens_per_s": 16 / td, "seconds": round(td, 3)}}
+
+
+def reference_arm(args, rank):
+    if rank != 0:
+        return
+    T_SAMPLE, B_SAMPLE = 64, 8
+    pre, dec = _oracle_prefill_sample(T_SAMPLE), _oracle_decode_sample(B_SAMPLE)
+    for _ in range(args.warmup):
+        pre(); dec()
+    tp = td = 0.0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        a = time.perf_counter(); pre(); b = time.perf_counter(); dec(); c = time.perf_counter()
+        tp += b - a
+        td += c - b
+    total = time.perf_counter() - t0
+    value = T_SAMPLE * args.steps / tp
+    dec_gbs = decode_state_bytes(B_SAMPLE) * args.steps / td / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample_per_step":
+                   f"oracle prefill of the first {T_SAMPLE} tokens (32 heads, gated norm) "
+                   f"+ oracle decode of {B_SAMPLE} sequences"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": f"{T_SAMPLE}-token prefill + "
+                         f"{B_SAMPLE}-sequence decode per step"},
+        "decode": {"value": dec_gbs, "unit": "GB/s"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+WORKLOAD = ("GDN core, Hq/Hk/Hv/D = 16/16/32/128: prefill of one T=2048 sequence with "
+            "gated-RMSNorm epilogue, zero initial state; decode of 256 sequences x 1 token, "
+            "fp32 states updated in place")
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        reference_arm(args, rank)
+        return
+
+    import gated_deltanet_linear_08_gb300 as gdn
+    from gated_deltanet_linear_08_gb300 import build as gbuild
+    gbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    gdn.load()
+
+    peaks = load_peaks()
+    pre = build_prefill_sets(dev, CASE_T2048, N_ROTATE)
+    dec_y, dec = build_decode(dev, CASE_DECODE)
+    stream = torch.cuda.Stream(device=dev)
+    x = pre[0]
+    T, hv = x["q"].shape[0], x["hv"]
+
+    with ClockSampler(local) as clk:
+        total_ms, pre_ms, dec_ms = timed_region(gdn, pre, dec, args.steps, args.warmup, stream,
+                                                world)
+    assert gdn.check_device_status() == 0
+    total_ms = max_over_ranks(total_ms, world)
+    pre_mean = max_over_ranks(sum(pre_ms) / len(pre_ms), world)
+    dec_mean = max_over_ranks(sum(dec_ms) / len(dec_ms), world)
+
+    flops = T * hv * PREFILL_FLOP_PER_TOKEN_HEAD
+    tflops = flops / (pre_mean * 1e-3) / 1e12
+    pre_bytes = T * (2 * 16 * 256 + 2 * hv * 256 + 2 * hv * 2 + hv * 256) + hv * 128 * 128 * 4
+    dbytes = decode_state_bytes(CASE_DECODE.batch)
+    dec_gbs = dbytes / (dec_mean * 1e-3) / 1e9
+
+    line = {
+        "metric": METRIC,
+        "value": world * T / (pre_mean * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": world,
+                   "seq_len": T, "decode_batch": CASE_DECODE.batch * world,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"prefill inputs rotated over {N_ROTATE} buffer sets (> L2); "
+                         "decode state 512 MiB (> L2)"},
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16"],
+                     "unit": "TFLOP/s", "frac": tflops / peaks["bf16"],
+                     "traffic": ncu_traffic("prefill"),
+                     "kernel": "gdn_prefill call (prep + scan kernels)",
+                     "peak_kind": f"{peaks['src']} bf16 burst",
+                     "work": f"{flops} algorithmic flop per call "
+                             f"({PREFILL_FLOP_PER_TOKEN_HEAD} per token per value head)"},
+        "prefill": {"ms_per_call": pre_mean, "algorithmic_bytes": pre_bytes,
+                    "hbm_gbs": pre_bytes / (pre_mean * 1e-3) / 1e9,
+                    "hbm_frac": pre_bytes / (pre_mean * 1e-3) / 1e9 / peaks["hbm"],
+                    "workspace_bytes": gdn.workspace_bytes(1, T, 16, hv)},
+        "decode": {"value": world * dec_gbs, "unit": "GB/s", "ms_per_call": dec_mean,
+                   "tokens_per_s": world * CASE_DECODE.batch / (dec_mean * 1e-3),
+                   "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm"],
+                                "unit": "GB/s", "frac": dec_gbs / peaks["hbm"],
+                                "frac_of_nominal_8tbs": dec_gbs / 8000.0,
+                                "traffic": ncu_traffic("decode"),
+                                "kernel": "decode_kernel",
+                                "peak_kind": f"{peaks['src']} HBM copy",
+                                "work": f"{dbytes} algorithmic bytes per call"}},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h = e2e_region(gdn, x, dec_y, dev, max(10, min(args.steps, 200)),
+                                      3, stream)
+        e2e_ms = max_over_ranks(e2e_ms, world)
+        line["e2e"] = {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": e2e_ms}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

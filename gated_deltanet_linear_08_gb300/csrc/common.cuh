@@ -1,10 +1,11 @@
 // common.cuh -- device helpers shared by the GDN kernels: the per-token gate
 // and beta (JevAny page "Add opt-in fused Qwen3.5 inference kernels",
-// Summary: gate from A_log and dt_bias, beta sigmoid), bf16 packing, and the
+// Summary: gate from A_log and dt_bias, beta sigmoid), bf16/fp16 packing, and the
 // device status bits that bounded waits set.
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace gdn {
 
@@ -15,6 +16,8 @@ constexpr float kL2Eps = 1e-6f;
 // Device status bits (OR-ed into the status word by kernels).
 constexpr uint32_t kStatusWaitTimeout = 1u << 0;
 constexpr uint32_t kStatusBadSeqlens = 1u << 1;
+constexpr uint32_t kStatusRange = 1u << 2;   // a value outside the fp16 operand range
+constexpr float kHalfMax = 65504.f;
 
 // softplus(x) = log(1 + e^x); above 20 the correction log1p(e^-x) < 2.1e-9
 // is below fp32 resolution of x, so x itself is returned.
@@ -47,6 +50,20 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi)
 {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ uint4 pack8(const float (&v)[8])
+{
+    return make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
+}
+// Pack two floats into f16x2 (round to nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t pack2h(float lo, float hi)
+{
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ uint4 pack8h(const float (&v)[8])
+{
+    return make_uint4(pack2h(v[0], v[1]), pack2h(v[2], v[3]), pack2h(v[4], v[5]), pack2h(v[6], v[7]));
 }
 __device__ __forceinline__ uint16_t bf16_bits(float x)
 {

@@ -8,21 +8,24 @@
 //
 // Per chunk (L <= 64 valid rows; padded rows are zero and change nothing),
 // with r_k, r_q the inverse L2 norms, g/beta the gate and beta, G the in-chunk
-// cumulative gate, Gam_i = e^{G_i}:
-//   D_a  = [K; Q] K^T                      raw bf16 q/k (exact), tcgen05
+// cumulative gate, Gam_i = e^{G_i}, Kn = diag(r_k) K:
+//   D_a  = [K; Q] K^T                       raw bf16 q/k (exact), tcgen05
 //   A_ij = beta_i e^{G_i-G_j} r_ki r_kj (K K^T)_ij      (j < i)
 //   P_ij = e^{G_i-G_j} r_qi r_kj (Q K^T)_ij             (j <= i)
-//   T    = (I + A)^{-1}                    fp32, blocked 16x16 substitution
-//   MT   = [T diag(beta); P T diag(beta)]  tcgen05, hi/lo-split bf16 operands
-//   [W; R] = MT diag(Gam r_k) K            tcgen05, raw K as exact operand
+//   T    = (I + A)^{-1}                     fp32, blocked 16x16 substitution
+//   MT   = [I; P] T diag(beta)              tcgen05, fp16 operands
+//   [W; R] = MT diag(Gam) Kn                tcgen05, fp16 operands
 //   WQ   = [-W; diag(Gam r_q) Q - R]
-// and it writes, in the 128-byte swizzled K-major byte image the scan kernel
-// copies straight into shared memory:
-//   WQ (128x128), MT (128x64), V^T (128 dv x 64 tokens), K^T (128 dk x 64,
-//   once per key head) and the row scales e^{G_last - G_i} r_ki, e^{G_last}.
-// The algebra: with U = Ut - W S0 (Ut = T diag(beta) V) the chunk's outputs
-// are scale (P Ut + (diag(Gam) Qn - P W) S0) = scale ([MT V]_bottom + [WQ S0]_bottom)
-// and U = [MT V]_top + [WQ S0]_top, so the serial scan needs one accumulator.
+// and it writes, as the fp16 swizzled byte images the scan kernel copies
+// straight into shared memory: WQ (128x128), MT (128x64), V (four [token][32]
+// value slices), Kn ([token][dk], once per key head) and the row scales
+// e^{G_last - G_i} and e^{G_last}.
+// With U = T diag(beta) V - W S0 the chunk's outputs are
+//   scale (P T diag(beta) V + (diag(Gam) Qn - P W) S0) = scale [MT V + WQ S0]_bottom
+// and U = [MT V + WQ S0]_top, so the serial scan needs one accumulator.
+// fp16 operands (10-bit mantissa) keep the rounding of the state-side
+// products 8x below bf16's; the bf16 inputs convert exactly.  A value of v
+// outside the fp16 range sets the range status bit.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc05.cuh"
@@ -33,19 +36,23 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kApad = 65;   // fp32 row stride of the A/T matrix (bank-conflict free)
 
-// Shared-memory map (offsets from a 1024-byte aligned base).
-constexpr uint32_t kOffKQ = 0;          // [K;Q] raw, 2 halves x 128 rows x 128 B
-constexpr uint32_t kOffA = 0;           //   reused after D_a: fp32 A/T [64][65]
-constexpr uint32_t kOffX = 16640;       //   reused after D_a: fp32 X [16][48]
-constexpr uint32_t kOffKT = 32768;      // K^T raw, 128 rows x 128 B
-constexpr uint32_t kOffAhi = 49152;     // [I; P_hi]   (V^T image before that)
-constexpr uint32_t kOffAlo = 65536;     // [0; P_lo]   (A' after MT is built)
-constexpr uint32_t kOffBhi = 81920;     // (T diag(beta))^T hi, 64 rows x 128 B
-constexpr uint32_t kOffBlo = 90112;     // (T diag(beta))^T lo
-constexpr uint32_t kOffSmall = 98304;   // per-row scalars, barrier, TMEM slot
+// Shared-memory map (offsets from a 1024-byte aligned base), ~51 KB so that
+// four CTAs share an SM.  Region R0 is reused as the kernel goes:
+//   [K;Q] bf16 image (until D_a completes)
+//   -> fp32 A/T [64][65], fp32 X [16][48], fp16 (T diag(beta))^T
+//   -> fp16 Kn image (after T diag(beta) has been consumed by the MT product)
+constexpr uint32_t kOffKQ = 0;          // bf16 [K;Q] raw, 2 halves x 128 rows x 128 B
+constexpr uint32_t kOffA = 0;           // fp32 A, then T, [64][65]
+constexpr uint32_t kOffX = 16640;       // fp32 X [16][48] of the blocked inverse
+constexpr uint32_t kOffTb = 20480;      // fp16 (T diag(beta))^T, 64 rows x 128 B
+constexpr uint32_t kOffKn = 0;          // fp16 Kn [token][dk], dk halves of 8 KB
+constexpr uint32_t kOffP = 32768;       // fp16 [I; P], 128 rows x 128 B; then A'
+constexpr uint32_t kOffSmall = 49152;   // per-row scalars, barrier, TMEM slot
 constexpr uint32_t kSmemBytes = kOffSmall + 2048 + 1024;  // + alignment slack
 
-constexpr uint32_t kTmemCols = 256;     // [0,64) D_a  [64,128) MT  [128,256) [W;R]
+// TMEM: D_a in [0,64), MT in [64,128); [W; R] reuses [0,128) once both have
+// been read.
+constexpr uint32_t kTmemCols = 128;
 
 struct Small {
     float rk[64], rq[64], G[64], gam[64], beta[64];
@@ -54,9 +61,9 @@ struct Small {
     int fail;
 };
 
-// Locate global chunk `gc`: sequence n, first token, valid rows.  Returns
-// false when gc lies past the last chunk.  Malformed cu_seqlens (decreasing
-// or outside [0, T]) are clamped to empty sequences and flagged.
+// Locate global chunk `gc`: first token and valid rows.  Returns false when gc
+// lies past the last chunk.  Malformed cu_seqlens (decreasing or outside
+// [0, T]) are treated as empty sequences and flagged.
 __device__ bool locate_chunk(const PrefillArgs &p, int gc, int &tok0, int &L, bool &bad)
 {
     int c = 0;
@@ -93,6 +100,46 @@ __device__ __forceinline__ void wait_mma(Small *sm, uint32_t parity, uint32_t *s
 // Inverse of the unit lower-triangular (I + A), in place in fp32 (row stride
 // kApad).  16x16 diagonal blocks by forward substitution (one thread per
 // column), then block rows a = 1..3: X = sum_c A_ac T_cb, T_ab = -T_aa X.
+template <int a>
+__device__ __forceinline__ void invert_block_row(float *A, float *X, int tid)
+{
+    constexpr int ncols = 16 * a;                    // columns 0 .. 16a-1
+    constexpr int per = 16 * ncols / kThreads;       // outputs per thread (2, 4, 6)
+    static_assert(16 * ncols % kThreads == 0, "outputs divide evenly");
+    // X[r][col] = sum over blocks b = col/16 .. a-1 of A[16a+r][16b..] T[16b..][col]
+#pragma unroll
+    for (int k = 0; k < per; ++k) {
+        const int e = tid + k * kThreads;
+        const int r = e / ncols, col = e % ncols, cb = col >> 4;
+        const float *arow = A + (16 * a + r) * kApad;
+        float acc = 0.f;
+#pragma unroll
+        for (int b = 0; b < a; ++b) {
+            if (b >= cb) {
+#pragma unroll
+                for (int m = 0; m < 16; ++m)
+                    acc = fmaf(arow[16 * b + m], A[(16 * b + m) * kApad + col], acc);
+            }
+        }
+        X[r * 48 + col] = acc;
+    }
+    __syncthreads();
+    // T[16a+r][col] = -sum_m T_aa[r][m] X[m][col]; T_aa's upper part is stored
+    // as zeros, so the sum runs over all 16 m
+#pragma unroll
+    for (int k = 0; k < per; ++k) {
+        const int e = tid + k * kThreads;
+        const int r = e / ncols, col = e % ncols;
+        const float *trow = A + (16 * a + r) * kApad + 16 * a;
+        float acc = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m)
+            acc = fmaf(trow[m], X[m * 48 + col], acc);
+        A[(16 * a + r) * kApad + col] = -acc;
+    }
+    __syncthreads();
+}
+
 __device__ void invert_unit_lower(float *A, float *X, int tid)
 {
     const int b = (tid >> 4) & 3, l = tid & 15, o = b * 16;
@@ -114,29 +161,12 @@ __device__ void invert_unit_lower(float *A, float *X, int tid)
             A[(o + i) * kApad + o + l] = x[i];
     }
     __syncthreads();
-    for (int a = 1; a < 4; ++a) {
-        const int ncols = 16 * a;              // columns 0 .. 16a-1
-        for (int e = tid; e < 16 * ncols; e += kThreads) {
-            const int r = e / ncols, col = e % ncols;
-            const int j0 = (col >> 4) << 4;    // first row of block b = col/16
-            float acc = 0.f;
-            for (int j = j0; j < 16 * a; ++j)
-                acc = fmaf(A[(16 * a + r) * kApad + j], A[j * kApad + col], acc);
-            X[r * 48 + col] = acc;
-        }
-        __syncthreads();
-        for (int e = tid; e < 16 * ncols; e += kThreads) {
-            const int r = e / ncols, col = e % ncols;
-            float acc = 0.f;
-            for (int m = 0; m <= r; ++m)
-                acc = fmaf(A[(16 * a + r) * kApad + 16 * a + m], X[m * 48 + col], acc);
-            A[(16 * a + r) * kApad + col] = -acc;
-        }
-        __syncthreads();
-    }
+    invert_block_row<1>(A, X, tid);
+    invert_block_row<2>(A, X, tid);
+    invert_block_row<3>(A, X, tid);
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 4)
 prep_kernel(PrefillArgs p)
 {
     const int gc = blockIdx.x, h = blockIdx.y;
@@ -157,13 +187,12 @@ prep_kernel(PrefillArgs p)
     Small *s = reinterpret_cast<Small *>(sm + kOffSmall);
     const uint32_t sbase = smem_u32(sm);
 
-    unsigned char *ws_v = p.workspace + ((size_t)gc * hv + h) * kPerVHead;
-    unsigned char *ws_wq = ws_v;
-    unsigned char *ws_mt = ws_v + kWQBytes;
-    unsigned char *ws_vt = ws_mt + kMTBytes;
-    float *ws_scal = reinterpret_cast<float *>(ws_vt + kVTBytes);
-    unsigned char *ws_kt = p.workspace + (size_t)p.max_chunks * hv * kPerVHead
-                           + ((size_t)gc * hk + hq) * kKTBytes;
+    unsigned char *ws_wq = p.workspace + ((size_t)gc * hv + h) * kPerVHead;
+    unsigned char *ws_mt = ws_wq + kWQBytes;
+    unsigned char *ws_vimg = ws_mt + kMTBytes;
+    float *ws_scal = reinterpret_cast<float *>(ws_vimg + kVBytes);
+    unsigned char *ws_k = p.workspace + (size_t)p.max_chunks * hv * kPerVHead
+                          + ((size_t)gc * hk + hq) * kKBytes;
 
     if (tid == 0) {
         mbar_init(&s->mbar, 1);
@@ -176,8 +205,9 @@ prep_kernel(PrefillArgs p)
         tc_fence_before();
     }
 
-    // ---- 1. raw K, Q (rows 0-63 K, 64-127 Q) -> [K;Q] image, K^T image,
-    //         sums of squares; V -> V^T image.  16 threads per 256-byte row.
+    // ---- 1. raw K, Q (rows 0-63 K, 64-127 Q) -> bf16 [K;Q] image and sums of
+    //         squares; V -> four fp16 [token][32] value-slice images in the
+    //         workspace.  16 threads per 256-byte row.
     const __nv_bfloat16 *qg = reinterpret_cast<const __nv_bfloat16 *>(p.q);
     const __nv_bfloat16 *kg = reinterpret_cast<const __nv_bfloat16 *>(p.k);
     const __nv_bfloat16 *vg = reinterpret_cast<const __nv_bfloat16 *>(p.v);
@@ -206,25 +236,25 @@ prep_kernel(PrefillArgs p)
             }
             *reinterpret_cast<uint4 *>(sm + kOffKQ + (chunk >> 3) * 16384
                                        + sw128_chunk_offset(r, chunk & 7)) = u;
-            if (r < 64) {
-                const uint16_t *hw = reinterpret_cast<const uint16_t *>(&u);
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    *reinterpret_cast<uint16_t *>(sm + kOffKT + sw128_offset(chunk * 8 + e, i)) = hw[e];
-            }
         }
+        bool over = false;
         for (int m = 0; m < 8; ++m) {
             const int i = (tid >> 4) + 8 * m;      // token 0..63
             uint4 u = make_uint4(0, 0, 0, 0);
             if (i < L)
                 u = *reinterpret_cast<const uint4 *>(vg + ((size_t)(tok0 + i) * hv + h) * kD + chunk * 8);
-            const uint16_t *hw = reinterpret_cast<const uint16_t *>(&u);
+            float f[8];
+            unpack8(u, f);
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                *reinterpret_cast<uint16_t *>(sm + kOffAhi + sw128_offset(chunk * 8 + e, i)) = hw[e];
+                over |= !(fabsf(f[e]) <= kHalfMax);
+            // value columns 8*chunk..+7 sit in slice chunk/4, 16-byte chunk chunk%4
+            *reinterpret_cast<uint4 *>(ws_vimg + (chunk >> 2) * 4096 + sw64_chunk_offset(i, chunk & 3)) = pack8h(f);
         }
+        if (over)
+            set_status(p.status, kStatusRange);
     }
-    // ---- 2. gates: g, beta, in-chunk inclusive cumsum G, Gam = e^G
+    // ---- 2. gates: g, beta, in-chunk inclusive cumsum G
     if (tid < 64) {
         float gv = 0.f, bv = 0.f;
         if (tid < L) {
@@ -246,7 +276,7 @@ prep_kernel(PrefillArgs p)
     if (tid >= 32 && tid < 64)
         s->G[tid] += s->G[31];
     if (warp == 0) {
-        // the MMA reads [K;Q] and K (rows 0-63 of the same image)
+        // D_a = [K;Q] K^T in bf16: the B operand is the K rows of the same image
         tc_fence_after();
         if (lane == 0) {
             const uint32_t d = s->tmem_base;   // columns [0, 64)
@@ -254,79 +284,64 @@ prep_kernel(PrefillArgs p)
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t off = kOffKQ + (kk >> 2) * 16384 + (kk & 3) * 32;
-                mma_bf16(d, make_sw128_desc(sbase + off), make_sw128_desc(sbase + off), idesc, kk > 0);
+                mma_f16(d, make_sw128_desc(sbase + off), make_sw128_desc(sbase + off), idesc, kk > 0);
             }
             mma_commit(&s->mbar);
         }
         __syncwarp();
     }
-    // V^T image and K^T image out to the workspace (16-byte coalesced)
-    for (int e = tid; e < 1024; e += kThreads) {
-        reinterpret_cast<uint4 *>(ws_vt)[e] = reinterpret_cast<const uint4 *>(sm + kOffAhi)[e];
-        if (h % group == 0)
-            reinterpret_cast<uint4 *>(ws_kt)[e] = reinterpret_cast<const uint4 *>(sm + kOffKT)[e];
-    }
-    __syncthreads();
+    __syncthreads();   // G complete before gam
     if (tid < 64)
         s->gam[tid] = expf(s->G[tid]);
     wait_mma(s, 0, p.status);
     tc_fence_after();
 
-    // ---- 3. A (fp32, rows 0-63) and P split hi/lo (bf16 rows 64-127 of the
-    //         [I; P_hi] and [0; P_lo] operands).
+    // ---- 3. A (fp32, rows 0-63) and P (fp16, rows 64-127 of [I; P]); A
+    //         overwrites the [K;Q] image, which D_a has finished reading.
+    //         Columns are taken 32 at a time to bound register use.
     float *sA = reinterpret_cast<float *>(sm + kOffA);
     float *sX = reinterpret_cast<float *>(sm + kOffX);
     {
-        float d[64];
-        {
-            float t0[32], t1[32];
-            const uint32_t ta = s->tmem_base + ((uint32_t)(warp * 32) << 16);
-            tmem_ld32(ta, t0);
-            tmem_ld32(ta + 32, t1);
+        const uint32_t ta = s->tmem_base + ((uint32_t)(warp * 32) << 16);
+        const int i = tid & 63;
+        const float Gi = s->G[i];
+        const float ci = (tid < 64) ? s->beta[i] * s->rk[i] : s->rq[i];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) { d[j] = t0[j]; d[32 + j] = t1[j]; }
+        for (int half = 0; half < 2; ++half) {
+            float d[32];
+            tmem_ld32(ta + half * 32, d);
+            if (tid < 64) {
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int j = half * 32 + jj;
+                    sA[i * kApad + j] = (j < i) ? ci * __expf(Gi - s->G[j]) * s->rk[j] * d[jj] : 0.f;
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float pv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int j = half * 32 + c * 8 + e;
+                        pv[e] = (j <= i) ? ci * __expf(Gi - s->G[j]) * s->rk[j] * d[c * 8 + e] : 0.f;
+                    }
+                    *reinterpret_cast<uint4 *>(sm + kOffP + sw128_chunk_offset(64 + i, half * 4 + c)) = pack8h(pv);
+                }
+            }
         }
-        if (tid < 64) {
-            const int i = tid;
-            const float Gi = s->G[i], ci = s->beta[i] * s->rk[i];
-#pragma unroll
-            for (int j = 0; j < 64; ++j)
-                sA[i * kApad + j] = (j < i) ? ci * expf(Gi - s->G[j]) * s->rk[j] * d[j] : 0.f;
-            // identity rows of [I; P_hi], zero rows of [0; P_lo]
+        if (tid < 64) {   // identity rows of [I; P]
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 uint32_t w[4] = {0, 0, 0, 0};
                 if ((i >> 3) == c)
-                    w[(i & 7) >> 1] = (i & 1) ? 0x3F800000u : 0x00003F80u;
-                *reinterpret_cast<uint4 *>(sm + kOffAhi + sw128_chunk_offset(i, c)) = make_uint4(w[0], w[1], w[2], w[3]);
-                *reinterpret_cast<uint4 *>(sm + kOffAlo + sw128_chunk_offset(i, c)) = make_uint4(0, 0, 0, 0);
-            }
-        } else {
-            const int i = tid - 64;
-            const float Gi = s->G[i], ci = s->rq[i];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint32_t whi[4], wlo[4];
-#pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    float pv[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int j = c * 8 + e + u;
-                        pv[u] = (j <= i) ? ci * expf(Gi - s->G[j]) * s->rk[j] * d[j] : 0.f;
-                    }
-                    const float h0 = bf16_round(pv[0]), h1 = bf16_round(pv[1]);
-                    whi[e >> 1] = pack2(h0, h1);
-                    wlo[e >> 1] = pack2(pv[0] - h0, pv[1] - h1);
-                }
-                *reinterpret_cast<uint4 *>(sm + kOffAhi + sw128_chunk_offset(64 + i, c)) = make_uint4(whi[0], whi[1], whi[2], whi[3]);
-                *reinterpret_cast<uint4 *>(sm + kOffAlo + sw128_chunk_offset(64 + i, c)) = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
+                    w[(i & 7) >> 1] = (i & 1) ? 0x3C000000u : 0x00003C00u;   // fp16 1.0
+                *reinterpret_cast<uint4 *>(sm + kOffP + sw128_chunk_offset(i, c)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
         }
     }
     __syncthreads();
 
-    // ---- 4. T = (I + A)^{-1} in fp32, then (T diag(beta))^T split hi/lo.
+    // ---- 4. T = (I + A)^{-1} in fp32, then (T diag(beta))^T in fp16
     invert_unit_lower(sA, sX, tid);
     {
         const int l = tid & 63, jh = tid >> 6;
@@ -334,82 +349,93 @@ prep_kernel(PrefillArgs p)
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
             const int c = jh * 4 + cc;
-            uint32_t whi[4], wlo[4];
+            float v[8];
 #pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-                const float v0 = sA[(c * 8 + e) * kApad + l] * bl;
-                const float v1 = sA[(c * 8 + e + 1) * kApad + l] * bl;
-                const float h0 = bf16_round(v0), h1 = bf16_round(v1);
-                whi[e >> 1] = pack2(h0, h1);
-                wlo[e >> 1] = pack2(v0 - h0, v1 - h1);
-            }
-            *reinterpret_cast<uint4 *>(sm + kOffBhi + sw128_chunk_offset(l, c)) = make_uint4(whi[0], whi[1], whi[2], whi[3]);
-            *reinterpret_cast<uint4 *>(sm + kOffBlo + sw128_chunk_offset(l, c)) = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
+            for (int e = 0; e < 8; ++e)
+                v[e] = sA[(c * 8 + e) * kApad + l] * bl;
+            *reinterpret_cast<uint4 *>(sm + kOffTb + sw128_chunk_offset(l, c)) = pack8h(v);
         }
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
 
-    // ---- 5. MT = [I; P_hi] Tb_hi + [I; P_hi] Tb_lo + [0; P_lo] Tb_hi  (fp32 in TMEM)
+    // ---- 5. MT = [I; P] T diag(beta)   (fp32 in TMEM columns 64..127)
     if (warp == 0) {
         tc_fence_after();
         if (lane == 0) {
             const uint32_t d = s->tmem_base + 64;
-            constexpr uint32_t idesc = make_idesc_bf16(128, 64);
-            const uint32_t aoff[3] = {kOffAhi, kOffAhi, kOffAlo};
-            const uint32_t boff[3] = {kOffBhi, kOffBlo, kOffBhi};
+            constexpr uint32_t idesc = make_idesc_f16(128, 64);
 #pragma unroll
-            for (int t = 0; t < 3; ++t)
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(d, make_sw128_desc(sbase + aoff[t] + kk * 32),
-                             make_sw128_desc(sbase + boff[t] + kk * 32), idesc, (t | kk) != 0);
+            for (int kk = 0; kk < 4; ++kk)
+                mma_f16(d, make_sw128_desc(sbase + kOffP + kk * 32),
+                        make_sw128_desc(sbase + kOffTb + kk * 32), idesc, kk != 0);
             mma_commit(&s->mbar);
         }
         __syncwarp();
     }
+    // Kn = diag(r_k) K in fp16, [token][dk] in dk halves of 8 KB (the operand
+    // layout of [W; R] below and of the scan kernel's state update), built
+    // from a second read of K while the MMA runs; it overwrites A, which is
+    // no longer needed (T diag(beta) lives elsewhere)
+    for (int e = tid; e < 1024; e += kThreads) {
+        const int half = e >> 9, i = (e >> 3) & 63, cc = e & 7;
+        float f[8];
+        if (i < L) {
+            unpack8(*reinterpret_cast<const uint4 *>(kg + ((size_t)(tok0 + i) * hk + hq) * kD + half * 64 + cc * 8), f);
+            const float rk = s->rk[i];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] *= rk;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = 0.f;
+        }
+        const uint4 hv8 = pack8h(f);
+        const uint32_t off = sw128_chunk_offset(i, cc);
+        *reinterpret_cast<uint4 *>(sm + kOffKn + half * 8192 + off) = hv8;
+        if (h % group == 0)
+            *reinterpret_cast<uint4 *>(ws_k + half * 8192 + off) = hv8;
+    }
     wait_mma(s, 1, p.status);
     tc_fence_after();
 
-    // ---- 6. MT row t -> workspace (bf16 image); A' = MT diag(Gam r_k) -> smem
+    // ---- 6. MT row t -> workspace (fp16 image); A' = MT diag(Gam) -> smem
+    //         (A' reuses the [I; P] buffer: the MMA that read it has completed)
     {
-        float mrow[64];
-        {
-            float t0[32], t1[32];
-            const uint32_t ta = s->tmem_base + ((uint32_t)(warp * 32) << 16) + 64;
-            tmem_ld32(ta, t0);
-            tmem_ld32(ta + 32, t1);
+        const uint32_t ta = s->tmem_base + ((uint32_t)(warp * 32) << 16) + 64;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) { mrow[j] = t0[j]; mrow[32 + j] = t1[j]; }
-        }
+        for (int half = 0; half < 2; ++half) {
+            float mrow[32];
+            tmem_ld32(ta + half * 32, mrow);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            uint32_t wm[4], wa[4];
+            for (int c = 0; c < 4; ++c) {
+                float m8[8], a8[8];
 #pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-                const int j = c * 8 + e;
-                wm[e >> 1] = pack2(mrow[j], mrow[j + 1]);
-                wa[e >> 1] = pack2(mrow[j] * s->gam[j] * s->rk[j], mrow[j + 1] * s->gam[j + 1] * s->rk[j + 1]);
+                for (int e = 0; e < 8; ++e) {
+                    m8[e] = mrow[c * 8 + e];
+                    a8[e] = m8[e] * s->gam[half * 32 + c * 8 + e];
+                }
+                *reinterpret_cast<uint4 *>(ws_mt + sw128_chunk_offset(tid, half * 4 + c)) = pack8h(m8);
+                *reinterpret_cast<uint4 *>(sm + kOffP + sw128_chunk_offset(tid, half * 4 + c)) = pack8h(a8);
             }
-            *reinterpret_cast<uint4 *>(ws_mt + sw128_chunk_offset(tid, c)) = make_uint4(wm[0], wm[1], wm[2], wm[3]);
-            *reinterpret_cast<uint4 *>(sm + kOffAlo + sw128_chunk_offset(tid, c)) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
         }
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
 
-    // ---- 7. [W; R] = A' K  (B operand: K^T image, N = 128 key dims)
+    // ---- 7. [W; R] = A' Kn into TMEM columns 0..127 (D_a and MT have been
+    //         read).  B = Kn read MN-major: dk halves 8 KB apart, 8-token
+    //         groups 1024 bytes apart; N = 128 key dims.
     if (warp == 0) {
         tc_fence_after();
         if (lane == 0) {
-            const uint32_t d = s->tmem_base + 128;
-            constexpr uint32_t idesc = make_idesc_bf16(128, 128);
+            const uint32_t d = s->tmem_base;
+            constexpr uint32_t idesc = make_idesc_f16(128, 128, false, true);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(d, make_sw128_desc(sbase + kOffAlo + kk * 32),
-                         make_sw128_desc(sbase + kOffKT + kk * 32), idesc, kk != 0);
+                mma_f16(d, make_sw128_desc(sbase + kOffP + kk * 32),
+                        make_desc(sbase + kOffKn + kk * 2048, 8192, 1024, kSw128), idesc, kk != 0);
             mma_commit(&s->mbar);
         }
         __syncwarp();
@@ -417,7 +443,7 @@ prep_kernel(PrefillArgs p)
     // row scales for the state update while the MMA runs
     if (tid < 64) {
         const float Gl = s->G[63];
-        ws_scal[tid] = (tid < L) ? expf(Gl - s->G[tid]) * s->rk[tid] : 0.f;
+        ws_scal[tid] = (tid < L) ? expf(Gl - s->G[tid]) : 0.f;
         if (tid == 0)
             ws_scal[64] = expf(Gl);
     }
@@ -430,35 +456,21 @@ prep_kernel(PrefillArgs p)
         const float qs = (tid >= 64) ? s->gam[i] * s->rq[i] : 0.f;
         for (int gq = 0; gq < 4; ++gq) {
             float dv[32];
-            tmem_ld32(s->tmem_base + ((uint32_t)(warp * 32) << 16) + 128 + gq * 32, dv);
-            float qv[32];
-            if (tid >= 64 && i < L) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(qg + ((size_t)(tok0 + i) * hk + hq) * kD + gq * 32);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    float f[8];
-                    unpack8(src[u], f);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) qv[u * 8 + e] = f[e];
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) qv[e] = 0.f;
-            }
+            tmem_ld32(s->tmem_base + ((uint32_t)(warp * 32) << 16) + gq * 32, dv);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                uint32_t w[4];
+                float qv[8];
+                if (tid >= 64 && i < L)
+                    unpack8(reinterpret_cast<const uint4 *>(qg + ((size_t)(tok0 + i) * hk + hq) * kD + gq * 32)[u], qv);
+                else
 #pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    const int j = u * 8 + e;
-                    float v0, v1;
-                    if (tid < 64) { v0 = -dv[j]; v1 = -dv[j + 1]; }
-                    else { v0 = fmaf(qs, qv[j], -dv[j]); v1 = fmaf(qs, qv[j + 1], -dv[j + 1]); }
-                    w[e >> 1] = pack2(v0, v1);
-                }
+                    for (int e = 0; e < 8; ++e) qv[e] = 0.f;
+                float w8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    w8[e] = (tid < 64) ? -dv[u * 8 + e] : fmaf(qs, qv[e], -dv[u * 8 + e]);
                 const int col = gq * 32 + u * 8;   // 0..127
-                *reinterpret_cast<uint4 *>(ws_wq + (col >> 6) * 16384 + sw128_chunk_offset(tid, (col & 63) >> 3))
-                    = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4 *>(ws_wq + (col >> 6) * 16384 + sw128_chunk_offset(tid, (col & 63) >> 3)) = pack8h(w8);
             }
         }
     }

@@ -10,15 +10,33 @@
 // parallel; with the epilogue on, the four CTAs of a head form a cluster and
 // exchange per-row sums of squares through distributed shared memory.
 //
-// Per chunk, with S the fp32 state slice (128 x 32) held in registers (thread
-// t owns key row t) and the chunk operands built by the prep kernel:
-//   X  = MT V + WQ S           one TMEM accumulator (tcgen05, M = 128)
-//   U  = X[0:64]               (= T diag(beta) V - W S)
-//   o  = X[64:128] / sqrt(Dk)  (= chunk outputs)
-//   Z  = K^T (diag(e^{G_last - G} r_k) U)   U split hi/lo bf16, raw K exact
+// Per chunk, with S the fp32 state slice (128 x 32) held in registers, and the
+// chunk operands built by the prep kernel (tcgen05, M = 128, fp16 operands):
+//   X  = MT V + WQ S                one TMEM accumulator
+//   U  = X[0:64]                    (= T diag(beta) V - W S)
+//   o  = X[64:128] / sqrt(Dk)       (= chunk outputs)
+//   Z  = Kn^T (diag(e^{G_last - G}) U)
 //   S  = e^{G_last} S + Z
-// Operands arrive by bulk asynchronous copy (one mbarrier per stage, two
-// stages); the next chunk's copy is in flight while this chunk computes.
+// Only WQ S and Z lie on the serial chain S -> X -> U -> Z -> S: MT V does not
+// depend on S and is issued after the previous chunk's Z when its operands
+// have already landed.  Operands stream through three stages; the copies for
+// chunk c+2 are issued, split over two threads, while Z(c) runs.  The tensor core accepts about one M=128 MMA per ~50
+// cycles at these widths, so the chain is counted in MMA instructions: 12 per
+// chunk.  The cluster exchange of row norms is deferred by one chunk and the
+// output stores follow the next cluster arrival, so neither the exchange nor
+// a store waits on the chain.
+//
+// 16 compute warps: warp w reads TMEM lane quadrant q = w % 4 and value
+// columns 8 (w / 4) .. +7 of each accumulator; thread (q, lane) owns state row
+// 32 q + lane.  Quadrants 0-1 form U (chunk rows 0-63), quadrants 2-3 the
+// outputs.  Every operand they write is MN-major, so each thread stores its 8
+// values as one 16-byte vector, then arrives on a named barrier without
+// waiting.  An issuer warp syncs on those barriers and issues every MMA, and a
+// loader warp issues the bulk copies, so no compute warp is held up issuing.
+// With the epilogue on, each CTA sums its row partials over its 32 columns
+// and pushes them into every cluster CTA's receive buffer with asynchronous
+// remote stores that complete bytes on the receiver's mbarrier: no
+// cluster-scope fence, no cluster-wide barrier per chunk.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc05.cuh"
@@ -29,50 +47,56 @@ cudaError_t launch_prefill_prep(const PrefillArgs &p, cudaStream_t stream);
 
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kComputeWarps = 16;
+constexpr int kIssuerWarp = kComputeWarps;        // issues every MMA
+constexpr int kLoaderWarp = kComputeWarps + 1;    // issues every bulk copy
+constexpr int kThreads = (kComputeWarps + 2) * 32;
+// Named barriers (id, participating threads): producers arrive, consumer warps
+// sync.
+constexpr uint32_t kBarS = 1, kCntS = kComputeWarps * 32 + 64;   // S operand written
+constexpr uint32_t kBarU = 2, kCntU = 8 * 32 + 32;               // U operand written
+constexpr uint32_t kBarRed = 3, kCntRed = 8 * 32;                // output warps' row partials
 constexpr int kNv = 32;                 // value columns per CTA
 constexpr int kTiles = kD / kNv;        // 4 CTAs per (sequence, head)
+constexpr int kCols = 8;                // value columns per thread
 
-// Stage layout (offsets within a stage; all 1024-byte aligned)
-constexpr uint32_t kStWQ = 0;           // 32 KB
-constexpr uint32_t kStMT = 32768;       // 16 KB
-constexpr uint32_t kStKT = 49152;       // 16 KB
-constexpr uint32_t kStVT = 65536;       //  4 KB (this CTA's 32 value rows)
+// Stage layout (offsets within a stage; all 1024-byte aligned).
+constexpr uint32_t kStWQ = 0;           // 32 KB  WQ, K-major, K halves of 16 KB
+constexpr uint32_t kStMT = 32768;       // 16 KB  MT, K-major
+constexpr uint32_t kStK = 49152;        // 16 KB  Kn [token][dk], MN-major A
+constexpr uint32_t kStV = 65536;        //  4 KB  V slice [token][32], MN-major B
 constexpr uint32_t kStScal = 69632;     //  272 B used
 constexpr uint32_t kScalCopy = 272;     //  65 floats rounded up to 16 bytes
 constexpr uint32_t kStageBytes = 70656;
-constexpr uint32_t kLoadBytes = 32768 + 16384 + 16384 + 4096 + kScalCopy;
+constexpr int kStages = 3;
+// bytes of the two halves of a stage's copies (one issuing thread each)
+constexpr uint32_t kLoadBytesA = (uint32_t)(kWQBytes + kMTBytes);
+constexpr uint32_t kLoadBytesB = (uint32_t)kKBytes + 4096 + kScalCopy;
 
-constexpr uint32_t kOffST = 2 * kStageBytes;        // S^T bf16: 2 halves x 32 rows x 128 B
-constexpr uint32_t kOffUhi = kOffST + 8192;         // (scaled U)^T hi: 32 rows x 128 B
-constexpr uint32_t kOffUlo = kOffUhi + 4096;
-constexpr uint32_t kOffSmall = kOffUlo + 4096;
-constexpr uint32_t kSmemBytes = kOffSmall + 1024 + 1024;
+constexpr uint32_t kOffS = kStages * kStageBytes;   // S operand [dk][32] fp16, MN-major, 8 KB
+constexpr uint32_t kOffU = kOffS + 8192;      // U operand [token][32] fp16, MN-major, 4 KB
+constexpr uint32_t kOffSmall = kOffU + 4096;
+constexpr uint32_t kSmemBytes = kOffSmall + 5120 + 1024;
 
-constexpr uint32_t kTmemCols = 128;     // X[2] at 0 and 32, Z at 64
+// TMEM columns: X[2] at 0 / 32, Z at 64.
+constexpr uint32_t kTmemCols = 128;
+constexpr uint32_t kColX = 0, kColZ = 64;
 
 constexpr float kScale = 0.088388347648318440550f;  // 1/sqrt(128)
 
 struct Small {
-    float red[2][64];       // per-row partial sums of squares (epilogue)
-    float w[kNv];           // gated-norm weight slice
-    uint64_t bar_load[2];
+    float red_local[2][4][64];  // row partial sums of squares [parity][column group][row]
+    float red_in[2][4][64];     // this CTA's row sums as received from [parity][cluster rank][row]
+    float w[kNv];               // gated-norm weight slice
+    uint64_t bar_load[kStages];   // two arrivals (one per issuing thread) + bytes
     uint64_t bar_x, bar_z;
+    uint64_t red_full[2];   // all cluster CTAs' row sums received (1 arrival + 1 KB)
     uint32_t tmem_base;
     int fail;
 };
 
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
-
-__device__ __forceinline__ float ld_peer_f32(const float *local, uint32_t rank)
-{
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
-}
 
 __device__ __forceinline__ bool wait_bar(Small *s, uint64_t *bar, uint32_t parity, uint32_t *status)
 {
@@ -86,7 +110,19 @@ __device__ __forceinline__ bool wait_bar(Small *s, uint64_t *bar, uint32_t parit
     return true;
 }
 
-// Chunks that precede sequence n, with the same clamping of malformed
+__device__ __forceinline__ bool wait_bar_cluster(Small *s, uint64_t *bar, uint32_t parity, uint32_t *status)
+{
+    if (*reinterpret_cast<volatile int *>(&s->fail))
+        return false;
+    for (uint32_t i = 0; i < kWaitPolls; ++i)
+        if (mbar_try_wait_cluster(bar, parity))
+            return true;
+    s->fail = 1;
+    set_status(status, kStatusWaitTimeout);
+    return false;
+}
+
+// Chunks that precede sequence n, with the same treatment of malformed
 // cu_seqlens as the prep kernel (a malformed sequence owns no chunks).
 __device__ int chunk_base_of(const PrefillArgs &p, int n, int &tok0, int &len)
 {
@@ -107,18 +143,36 @@ __device__ int chunk_base_of(const PrefillArgs &p, int n, int &tok0, int &len)
     return c;
 }
 
-__device__ __forceinline__ void issue_loads(const PrefillArgs &p, unsigned char *stage, uint64_t *bar,
-                                            int gc, int h, int hq, int r)
+// The stage's copies are split over two issuing threads: half A (WQ, MT) and
+// half B (Kn, the V slice, the row scales).
+__device__ __forceinline__ void issue_loads_a(const PrefillArgs &p, unsigned char *stage, uint64_t *bar,
+                                              int gc, int h)
+{
+    const unsigned char *wv = p.workspace + ((size_t)gc * p.hv + h) * kPerVHead;
+    mbar_arrive_expect_tx(bar, kLoadBytesA);
+    bulk_g2s(stage + kStWQ, wv, (uint32_t)kWQBytes, bar);
+    bulk_g2s(stage + kStMT, wv + kWQBytes, (uint32_t)kMTBytes, bar);
+}
+__device__ __forceinline__ void issue_loads_b(const PrefillArgs &p, unsigned char *stage, uint64_t *bar,
+                                              int gc, int h, int hq, int r)
 {
     const unsigned char *wv = p.workspace + ((size_t)gc * p.hv + h) * kPerVHead;
     const unsigned char *wk = p.workspace + (size_t)p.max_chunks * p.hv * kPerVHead
-                              + ((size_t)gc * p.hk + hq) * kKTBytes;
-    mbar_arrive_expect_tx(bar, kLoadBytes);
-    bulk_g2s(stage + kStWQ, wv, 32768, bar);
-    bulk_g2s(stage + kStMT, wv + kWQBytes, 16384, bar);
-    bulk_g2s(stage + kStKT, wk, 16384, bar);
-    bulk_g2s(stage + kStVT, wv + kWQBytes + kMTBytes + r * 4096, 4096, bar);
-    bulk_g2s(stage + kStScal, wv + kWQBytes + kMTBytes + kVTBytes, kScalCopy, bar);
+                              + ((size_t)gc * p.hk + hq) * kKBytes;
+    mbar_arrive_expect_tx(bar, kLoadBytesB);
+    bulk_g2s(stage + kStK, wk, (uint32_t)kKBytes, bar);
+    bulk_g2s(stage + kStV, wv + kWQBytes + kMTBytes + r * 4096, 4096, bar);
+    bulk_g2s(stage + kStScal, wv + kWQBytes + kMTBytes + kVBytes, kScalCopy, bar);
+}
+
+// X(stage) += MT V: four K steps over the 64 tokens.
+__device__ __forceinline__ void issue_mtv(uint32_t dx, uint32_t soff, uint32_t idesc)
+{
+    const uint64_t a = make_desc(soff + kStMT, 16, 1024, kSw128);
+    const uint64_t b = make_desc(soff + kStV, 512, 512, kSw64);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+        mma_f16(dx, a + (uint64_t)(kk * 2), b + (uint64_t)(kk * 64), idesc, kk != 0);
 }
 
 template <bool kNorm>
@@ -127,7 +181,7 @@ scan_kernel(PrefillArgs p)
 {
     const int r = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int hv = p.hv, hq = h / (hv / p.hk);
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
@@ -140,10 +194,12 @@ scan_kernel(PrefillArgs p)
     const int nck = (len + kC - 1) / kC;
 
     if (tid == 0) {
-        mbar_init(&s->bar_load[0], 1);
-        mbar_init(&s->bar_load[1], 1);
+        for (int i = 0; i < kStages; ++i)
+            mbar_init(&s->bar_load[i], 2);
         mbar_init(&s->bar_x, 1);
         mbar_init(&s->bar_z, 1);
+        mbar_init(&s->red_full[0], 1);
+        mbar_init(&s->red_full[1], 1);
         mbar_fence_init();
         s->fail = 0;
     }
@@ -156,194 +212,227 @@ scan_kernel(PrefillArgs p)
     }
     __syncthreads();
     tc_fence_after();
-    if (kNorm) {   // every CTA of the cluster has started before any DSMEM access
+    if (kNorm) {   // every CTA of the cluster is running before any DSMEM access
         cluster_arrive();
         cluster_wait();
     }
     const uint32_t tbase = s->tmem_base;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t idesc_x = make_idesc_f16(128, kNv, false, true);
+    const uint32_t idesc_z = make_idesc_f16(128, kNv, true, true);
 
-    // state slice: key row tid, value columns [32r, 32r+32)
-    const size_t srow = (((size_t)n * hv + h) * kD + tid) * kD + r * kNv;
-    float S[kNv];
-    if (p.init_state) {
-        const float4 *src = reinterpret_cast<const float4 *>(p.init_state + srow);
+    if (warp == kIssuerWarp) {
+        // ------------------------------------------------------------ issuer
+        const uint64_t desc_s = make_desc(sbase + kOffS, 512, 512, kSw64);
+        const uint64_t desc_u = make_desc(sbase + kOffU, 512, 512, kSw64);
+        bool mtv_pre = false;
+        for (int c = 0; c < nck; ++c) {
+            const int st = c % kStages;
+            const uint32_t soff = sbase + st * kStageBytes;
+            named_sync(kBarS, kCntS);            // S(c) operand written
+            if (lane == 0) {
+                if (wait_bar(s, &s->bar_load[st], (uint32_t)(c / kStages) & 1, p.status)) {
+                    tc_fence_after();
+                    const uint32_t dx = tbase + kColX + (c & 1) * kNv;
+                    if (!mtv_pre)
+                        issue_mtv(dx, soff, idesc_x);
+                    const uint64_t a = make_desc(soff + kStWQ, 16, 1024, kSw128);
 #pragma unroll
-        for (int j = 0; j < kNv / 4; ++j) {
-            const float4 x = src[j];
-            S[4 * j] = x.x; S[4 * j + 1] = x.y; S[4 * j + 2] = x.z; S[4 * j + 3] = x.w;
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_f16(dx, a + (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2),
+                                desc_s + (uint64_t)(kk * 64), idesc_x, 1);
+                }
+                mma_commit(&s->bar_x);
+            }
+            __syncwarp();
+            named_sync(kBarU, kCntU);            // U(c) operand written
+            if (lane == 0) {
+                if (!*reinterpret_cast<volatile int *>(&s->fail)) {
+                    tc_fence_after();
+                    const uint64_t a = make_desc(soff + kStK, 8192, 1024, kSw128);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_f16(tbase + kColZ, a + (uint64_t)(kk * 128), desc_u + (uint64_t)(kk * 64),
+                                idesc_z, kk != 0);
+                }
+                mma_commit(&s->bar_z);
+                mtv_pre = false;
+                if (c + 1 < nck && !*reinterpret_cast<volatile int *>(&s->fail)) {
+                    const int ns = (c + 1) % kStages;
+                    if (mbar_test(&s->bar_load[ns], (uint32_t)((c + 1) / kStages) & 1)) {
+                        tc_fence_after();
+                        issue_mtv(tbase + kColX + ((c + 1) & 1) * kNv, sbase + ns * kStageBytes, idesc_x);
+                        mtv_pre = true;
+                    }
+                }
+            }
+            __syncwarp();
+        }
+    } else if (warp == kLoaderWarp) {
+        // ------------------------------------------------------------ loader
+        int issued[kStages] = {0, 0, 0};
+        auto issue_stage = [&](int cc) {
+            const int st = cc % kStages;
+            issue_loads_a(p, sm + st * kStageBytes, &s->bar_load[st], cbase + cc, h);
+            issue_loads_b(p, sm + st * kStageBytes, &s->bar_load[st], cbase + cc, h, hq, r);
+            ++issued[st];
+        };
+        if (lane == 0)
+            for (int cc = 0; cc < 2 && cc < nck; ++cc)
+                issue_stage(cc);
+        for (int c = 0; c < nck; ++c) {
+            named_sync(kBarS, kCntS);
+            // chunk c+2 goes into the stage chunk c-1 used: Z(c-1) was read
+            // and every read of that stage's row scales happened before the
+            // S(c) barrier
+            if (lane == 0 && c + 2 < nck)
+                issue_stage(c + 2);
+            __syncwarp();
+        }
+        // no copy may still be landing in shared memory when the CTA exits
+        if (lane == 0 && *reinterpret_cast<volatile int *>(&s->fail)) {
+            for (int qq = 0; qq < kStages; ++qq)
+                if (issued[qq] > 0)
+                    mbar_wait(&s->bar_load[qq], (issued[qq] - 1) & 1);
         }
     } else {
+        // ------------------------------------------------------------ compute
+        const int q = warp & 3, g = warp >> 2;
+        const int row = 32 * q + lane;     // TMEM lane = state row = chunk row
+        const int orow = row - 64;         // output row for quadrants 2-3
+        const uint32_t tlane = tbase + ((uint32_t)(32 * q) << 16) + g * kCols;
+        const size_t sidx = (((size_t)n * hv + h) * kD + row) * kD + r * kNv + g * kCols;
+        const size_t col0 = (size_t)r * kNv + g * kCols;
+        const __nv_bfloat16 *zg = reinterpret_cast<const __nv_bfloat16 *>(p.z);
+        __nv_bfloat16 *outg = reinterpret_cast<__nv_bfloat16 *>(p.out);
+
+        float S[kCols];
+        if (p.init_state) {
+            const float4 a0 = reinterpret_cast<const float4 *>(p.init_state + sidx)[0];
+            const float4 a1 = reinterpret_cast<const float4 *>(p.init_state + sidx)[1];
+            S[0] = a0.x; S[1] = a0.y; S[2] = a0.z; S[3] = a0.w;
+            S[4] = a1.x; S[5] = a1.y; S[6] = a1.z; S[7] = a1.w;
+        } else {
 #pragma unroll
-        for (int j = 0; j < kNv; ++j) S[j] = 0.f;
-    }
-
-    int issued[2] = {0, 0};   // loads issued per stage (thread 0 only)
-    if (tid == 0 && nck > 0) {
-        issue_loads(p, sm, &s->bar_load[0], cbase, h, hq, r);
-        issued[0] = 1;
-    }
-
-    for (int ci = 0; ci < nck; ++ci) {
-        const int st = ci & 1;
-        unsigned char *stage = sm + st * kStageBytes;
-        const uint32_t soff = st * kStageBytes;
-        const int t0 = tok0 + ci * kC;
-        const int L = min(kC, tok0 + len - t0);
-
-        // (1) S -> bf16 S^T operand (value row j, key column tid)
-        {
-            const uint32_t off = kOffST + (tid >> 6) * 4096;
-#pragma unroll
-            for (int j = 0; j < kNv; ++j)
-                *reinterpret_cast<uint16_t *>(sm + off + sw128_offset(j, tid & 63)) = bf16_bits(S[j]);
+            for (int j = 0; j < kCols; ++j) S[j] = 0.f;
         }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
+        const uint32_t my_rank = kNorm ? cluster_ctarank() : 0;
+        float o_prev[kCols], z_prev[kCols];   // outputs of the previous chunk awaiting its norm
+#pragma unroll
+        for (int j = 0; j < kCols; ++j) { o_prev[j] = 0.f; z_prev[j] = 0.f; }
+        bool over = false;   // a state value left the fp16 operand range
 
-        // (2) prefetch the next chunk; X = MT V + WQ S
-        if (tid == 0) {
-            if (ci + 1 < nck) {
-                const int nst = (ci + 1) & 1;
-                issue_loads(p, sm + nst * kStageBytes, &s->bar_load[nst], cbase + ci + 1, h, hq, r);
-                ++issued[nst];
-            }
-            if (wait_bar(s, &s->bar_load[st], (ci >> 1) & 1, p.status)) {
-                tc_fence_after();
-                const uint32_t dx = tbase + st * kNv;
-                constexpr uint32_t idesc = make_idesc_bf16(128, kNv);
+        // gated RMSNorm and store of chunk c's output rows, once every CTA of
+        // the cluster has published its partial sums for them
+        auto finish = [&](int c) {
+            const int Lc = min(kC, len - c * kC);
+            const bool ok = wait_bar_cluster(s, &s->red_full[c & 1], (uint32_t)(c >> 1) & 1, p.status);
+            if (!ok || orow >= Lc)
+                return;
+            float tot = 0.f;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(dx, make_sw128_desc(sbase + soff + kStMT + kk * 32),
-                             make_sw128_desc(sbase + soff + kStVT + kk * 32), idesc, kk != 0);
+            for (int rk = 0; rk < kTiles; ++rk)
+                tot += s->red_in[c & 1][rk][orow];
+            const float rn = rsqrtf(tot * (1.f / kD) + p.eps);
+            float y[kCols];
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(dx, make_sw128_desc(sbase + soff + kStWQ + (kk >> 2) * 16384 + (kk & 3) * 32),
-                             make_sw128_desc(sbase + kOffST + (kk >> 2) * 4096 + (kk & 3) * 32), idesc, 1);
-            }
-            mma_commit(&s->bar_x);
-        }
-        __syncwarp();
+            for (int j = 0; j < kCols; ++j)
+                y[j] = o_prev[j] * rn * s->w[g * kCols + j] * (z_prev[j] * sigmoid_f(z_prev[j]));
+            *reinterpret_cast<uint4 *>(outg + ((size_t)(tok0 + c * kC + orow) * hv + h) * kD + col0) = pack8(y);
+        };
 
-        // z slice for the epilogue (loads overlap the MMA)
-        float zf[kNv];
-        const int i_out = tid - 64;
-        const bool row_ok = tid >= 64 && i_out < L;
-        if (kNorm) {
-            if (row_ok) {
-                const uint4 *zp = reinterpret_cast<const uint4 *>(
-                    reinterpret_cast<const __nv_bfloat16 *>(p.z) + ((size_t)(t0 + i_out) * hv + h) * kD + r * kNv);
+        for (int c = 0; c < nck; ++c) {
+            const int pp = c & 1;
+            const int st = c % kStages;
+            const int Lc = min(kC, len - c * kC);
+            const float *scal = reinterpret_cast<const float *>(sm + st * kStageBytes + kStScal);
+
+            // (A) state -> fp16 operand S
+            {
+                float v[kCols];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    float f[8];
-                    unpack8(zp[u], f);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) zf[u * 8 + e] = f[e];
+                for (int j = 0; j < kCols; ++j) {
+                    v[j] = S[j];
+                    over |= !(fabsf(S[j]) <= kHalfMax);
                 }
+                *reinterpret_cast<uint4 *>(sm + kOffS + sw64_chunk_offset(row, g)) = pack8h(v);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            named_arrive(kBarS, kCntS);
+
+            // (D) the previous chunk's outputs (their norms are complete by now)
+            if (kNorm && c >= 1 && q >= 2)
+                finish(c - 1);
+
+            // (C) U rows -> scaled operand; output rows -> epilogue
+            float zc[kCols];
+            if (kNorm && q >= 2 && orow < Lc) {   // z of this chunk, loaded under the MMA
+                unpack8(*reinterpret_cast<const uint4 *>(zg + ((size_t)(tok0 + c * kC + orow) * hv + h) * kD + col0), zc);
             } else {
 #pragma unroll
-                for (int e = 0; e < kNv; ++e) zf[e] = 0.f;
+                for (int j = 0; j < kCols; ++j) zc[j] = 0.f;
             }
-        }
+            wait_bar(s, &s->bar_x, pp, p.status);
+            wait_bar(s, &s->bar_load[st], (uint32_t)(c / kStages) & 1, p.status);   // row scales visible
+            tc_fence_after();
+            float xv[kCols];
+            tmem_ld8(tlane + kColX + pp * kNv, xv);
+            if (q < 2) {
+                const float sc = scal[row];
+                float u[kCols];
+#pragma unroll
+                for (int j = 0; j < kCols; ++j) u[j] = xv[j] * sc;
+                *reinterpret_cast<uint4 *>(sm + kOffU + sw64_chunk_offset(row, g)) = pack8h(u);
+                fence_async_smem();
+                tc_fence_before();
+                named_arrive(kBarU, kCntU);
+            } else {
+                float ss = 0.f;
+#pragma unroll
+                for (int j = 0; j < kCols; ++j) {
+                    o_prev[j] = xv[j] * kScale;
+                    ss = fmaf(o_prev[j], o_prev[j], ss);
+                    z_prev[j] = zc[j];
+                }
+                if (kNorm) {
+                    // row sums over this CTA's 32 columns, pushed to all four
+                    // CTAs' receive buffers (slot = this CTA's rank)
+                    s->red_local[pp][g][orow] = ss;
+                    named_sync(kBarRed, kCntRed);
+                    if (g == 0) {
+                        if (orow == 0)
+                            mbar_arrive_expect_tx(&s->red_full[pp], kTiles * 64 * 4);
+                        const float t = s->red_local[pp][0][orow] + s->red_local[pp][1][orow]
+                                      + s->red_local[pp][2][orow] + s->red_local[pp][3][orow];
+#pragma unroll
+                        for (uint32_t rk = 0; rk < kTiles; ++rk)
+                            st_async_remote(&s->red_in[pp][my_rank][orow], t, &s->red_full[pp], rk);
+                    }
+                } else if (orow < Lc) {
+                    *reinterpret_cast<uint4 *>(outg + ((size_t)(tok0 + c * kC + orow) * hv + h) * kD + col0) = pack8(o_prev);
+                }
+            }
 
-        // (3) U rows -> scaled hi/lo operand; output rows -> epilogue
-        wait_bar(s, &s->bar_x, ci & 1, p.status);
-        wait_bar(s, &s->bar_load[st], (ci >> 1) & 1, p.status);   // scal visibility
-        tc_fence_after();
-        float xv[kNv];
-        tmem_ld32(tbase + lane_base + st * kNv, xv);
-        const float *scal = reinterpret_cast<const float *>(stage + kStScal);
-        float o[kNv];
-        if (tid < 64) {
-            const float sc = scal[tid];
+            // (F) S = e^{G_last} S + Z
+            wait_bar(s, &s->bar_z, pp, p.status);
+            tc_fence_after();
+            float zv[kCols];
+            tmem_ld8(tlane + kColZ, zv);
+            const float gl = scal[64];
 #pragma unroll
-            for (int j = 0; j < kNv; ++j) {
-                const float u = xv[j] * sc;
-                const float hi = bf16_round(u);
-                *reinterpret_cast<uint16_t *>(sm + kOffUhi + sw128_offset(j, tid)) = bf16_bits(hi);
-                *reinterpret_cast<uint16_t *>(sm + kOffUlo + sw128_offset(j, tid)) = bf16_bits(u - hi);
-            }
-        } else {
-            float ss = 0.f;
-#pragma unroll
-            for (int j = 0; j < kNv; ++j) {
-                o[j] = xv[j] * kScale;
-                ss = fmaf(o[j], o[j], ss);
-            }
-            if (kNorm)
-                s->red[ci & 1][i_out] = ss;
+            for (int j = 0; j < kCols; ++j) S[j] = fmaf(gl, S[j], zv[j]);
         }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (kNorm)
-            cluster_arrive();
+        if (kNorm && nck >= 1 && q >= 2)
+            finish(nck - 1);
 
-        // (4) Z = K^T U_hi + K^T U_lo
-        if (tid == 0) {
-            if (!*reinterpret_cast<volatile int *>(&s->fail)) {
-                tc_fence_after();
-                const uint32_t dz = tbase + 2 * kNv;
-                constexpr uint32_t idesc = make_idesc_bf16(128, kNv);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(dz, make_sw128_desc(sbase + soff + kStKT + (kk & 3) * 32),
-                             make_sw128_desc(sbase + ((kk >> 2) ? kOffUlo : kOffUhi) + (kk & 3) * 32),
-                             idesc, kk != 0);
-            }
-            mma_commit(&s->bar_z);
-        }
-        __syncwarp();
-        if (tid >= 64) {
-            if (kNorm) {
-                cluster_wait();
-                float tot = 0.f;
-#pragma unroll
-                for (uint32_t q = 0; q < kTiles; ++q)
-                    tot += ld_peer_f32(&s->red[ci & 1][i_out], q);
-                const float rn = rsqrtf(tot * (1.f / kD) + p.eps);
-#pragma unroll
-                for (int j = 0; j < kNv; ++j)
-                    o[j] = o[j] * rn * s->w[j] * (zf[j] * sigmoid_f(zf[j]));
-            }
-            if (row_ok) {
-                uint4 *dst = reinterpret_cast<uint4 *>(
-                    reinterpret_cast<__nv_bfloat16 *>(p.out) + ((size_t)(t0 + i_out) * hv + h) * kD + r * kNv);
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    dst[u] = make_uint4(pack2(o[8 * u], o[8 * u + 1]), pack2(o[8 * u + 2], o[8 * u + 3]),
-                                        pack2(o[8 * u + 4], o[8 * u + 5]), pack2(o[8 * u + 6], o[8 * u + 7]));
-            }
-        }
-
-        // (5) S = e^{G_last} S + Z
-        wait_bar(s, &s->bar_z, ci & 1, p.status);
-        tc_fence_after();
-        float zv[kNv];
-        tmem_ld32(tbase + lane_base + 2 * kNv, zv);
-        const float gl = scal[64];
-#pragma unroll
-        for (int j = 0; j < kNv; ++j)
-            S[j] = fmaf(gl, S[j], zv[j]);
-        if (kNorm && tid < 64)
-            cluster_wait();
+        if (over)
+            set_status(p.status, kStatusRange);
+        float4 *dst = reinterpret_cast<float4 *>(p.final_state + sidx);
+        dst[0] = make_float4(S[0], S[1], S[2], S[3]);
+        dst[1] = make_float4(S[4], S[5], S[6], S[7]);
     }
 
-    // final state slice
-    {
-        float4 *dst = reinterpret_cast<float4 *>(p.final_state + srow);
-#pragma unroll
-        for (int j = 0; j < kNv / 4; ++j)
-            dst[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
-    }
-    // no copy may still be landing in shared memory when the CTA exits
-    if (tid == 0 && *reinterpret_cast<volatile int *>(&s->fail)) {
-        for (int q = 0; q < 2; ++q)
-            if (issued[q] > 0)
-                mbar_wait(&s->bar_load[q], (issued[q] - 1) & 1);
-    }
-    if (kNorm) {   // peers may still read this CTA's partial sums
+    if (kNorm) {   // peers may still be reading this CTA's partial sums
         cluster_arrive();
         cluster_wait();
     }

@@ -35,18 +35,22 @@ struct PrefillArgs {
 };
 
 // Workspace layout of the chunked prefill (all offsets 1024-byte aligned).
-// Per (chunk, value head):  WQ   bf16 128x128 (two 64-wide K halves), 32 KB
-//                           MT   bf16 128x64, 16 KB
-//                           VT   bf16 128(dv)x64(tokens), 16 KB
-//                           scal fp32: [0,64) state-update row scales,
-//                                [64] exp(G_last), padded to 1 KB
-// Per (chunk, key head):    KT   bf16 128(dk)x64(tokens), 16 KB
+// Images are byte-exact shared-memory operand layouts (see tc05.cuh), fp16.
+// Per (chunk, value head):  WQ   128x128, K-major 128B swizzle, two 64-wide K
+//                                halves of 16 KB, 32 KB
+//                           MT   128x64, K-major 128B swizzle, 16 KB
+//                           V    [token 64][dv 32] x 4 value slices,
+//                                MN-major 64B swizzle, 4 KB each, 16 KB
+//                           scal fp32: [0,64) state-update row scales
+//                                e^{G_last - G_i}, [64] e^{G_last}, 1 KB
+// Per (chunk, key head):    Kn   L2-normalised keys [token 64][dk 128],
+//                                MN-major 128B swizzle, dk halves of 8 KB
 constexpr size_t kWQBytes = 32768;
 constexpr size_t kMTBytes = 16384;
-constexpr size_t kVTBytes = 16384;
+constexpr size_t kVBytes = 16384;
 constexpr size_t kScalBytes = 1024;
-constexpr size_t kPerVHead = kWQBytes + kMTBytes + kVTBytes + kScalBytes;  // 66560
-constexpr size_t kKTBytes = 16384;
+constexpr size_t kPerVHead = kWQBytes + kMTBytes + kVBytes + kScalBytes;  // 66560
+constexpr size_t kKBytes = 16384;
 
 inline int prefill_max_chunks(int num_seqs, int total_tokens)
 {
@@ -57,7 +61,7 @@ inline size_t prefill_workspace_bytes(int num_seqs, int total_tokens, int hk, in
     if (total_tokens <= 0)
         return 0;
     const size_t c = (size_t)prefill_max_chunks(num_seqs, total_tokens);
-    return c * (size_t)hv * kPerVHead + c * (size_t)hk * kKTBytes;
+    return c * (size_t)hv * kPerVHead + c * (size_t)hk * kKBytes;
 }
 
 cudaError_t launch_decode(const DecodeArgs &args, cudaStream_t stream);

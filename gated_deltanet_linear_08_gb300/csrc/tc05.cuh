@@ -4,11 +4,13 @@
 // these instructions; nothing here is generated.
 //
 // Conventions used by every kernel in this library:
-//   * All MMA operands are bf16, K-major, in the 128-byte swizzled layout:
-//     rows of 128 bytes (64 bf16 along K), 8-row atoms of 1024 bytes, the
-//     16-byte chunk c of row r stored at chunk position c ^ (r & 7).  Atom
-//     bases are 1024-byte aligned.  Operands wider than 64 along K are split
-//     into 64-wide "halves", each a separate run of atoms.
+//   * MMA operands are 16-bit (bf16 or fp16) in swizzled shared-memory
+//     layouts: K-major or MN-major with 128-byte rows (64 elements; 8-row
+//     atoms of 1024 bytes, 16-byte chunk c of row r at position c ^ (r & 7)),
+//     or MN-major with 64-byte rows (32 elements; 8-row atoms of 512 bytes,
+//     chunk c of row r at c ^ ((r >> 1) & 3)).  Atom bases are aligned to the
+//     atom size.  Extents wider than one row are split into "halves", each a
+//     separate run of atoms.
 //   * Accumulators are fp32 in TMEM, M = 128 (lane i = row i).
 #pragma once
 #include <cstdint>
@@ -52,12 +54,55 @@ __device__ __forceinline__ uint64_t make_sw128_desc(uint32_t saddr)
     return d;
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B, fp32 D, both K-major.
-__host__ __device__ constexpr uint32_t make_idesc_bf16(uint32_t M, uint32_t N)
+// General form: layout 2 = 128-byte swizzle, 4 = 64-byte swizzle.
+//   K-major 128B:  rows of 64 K elements, SBO = 1024 between 8-row atoms.
+//   MN-major 128B: rows of 64 MN elements, one row per K index; SBO = 1024
+//                  between groups of 8 K rows, LBO = distance between
+//                  successive 64-wide MN blocks.
+//   MN-major 64B:  rows of 32 MN elements (64 bytes), one per K index;
+//                  SBO = 512 between groups of 8 K rows (atoms of 512 bytes).
+__device__ __forceinline__ uint64_t make_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t layout)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)layout << 61;
+    return d;
+}
+constexpr uint32_t kSw128 = 2, kSw64 = 4;
+
+// Byte offset of 16-byte chunk `chunk` (0..3) of row `row` in a 64-byte-row
+// swizzled tile (atoms of 8 rows x 64 bytes, 512-byte aligned).
+__device__ __forceinline__ uint32_t sw64_chunk_offset(uint32_t row, uint32_t chunk)
+{
+    return row * 64u + (((chunk ^ (row >> 1)) & 3u) << 4);
+}
+
+// Instruction descriptors for kind::f16 with fp32 D; both operands share one
+// type (bf16, or fp16).  a_mn / b_mn select MN-major (transposed) operands;
+// the default is K-major.
+__host__ __device__ constexpr uint32_t make_idesc_f16(uint32_t M, uint32_t N, bool a_mn = false,
+                                                      bool b_mn = false)
+{
+    return (1u << 4)            // D format: f32
+         | (0u << 7)            // A format: f16
+         | (0u << 10)           // B format: f16
+         | ((a_mn ? 1u : 0u) << 15)
+         | ((b_mn ? 1u : 0u) << 16)
+         | ((N >> 3) << 17)     // N / 8
+         | ((M >> 4) << 24);    // M / 16
+}
+__host__ __device__ constexpr uint32_t make_idesc_bf16(uint32_t M, uint32_t N, bool a_mn = false,
+                                                       bool b_mn = false)
 {
     return (1u << 4)            // D format: f32
          | (1u << 7)            // A format: bf16
          | (1u << 10)           // B format: bf16
+         | ((a_mn ? 1u : 0u) << 15)
+         | ((b_mn ? 1u : 0u) << 16)
          | ((N >> 3) << 17)     // N / 8
          | ((M >> 4) << 24);    // M / 16
 }
@@ -86,8 +131,9 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 // operand reads, bulk copies).
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// D[tmem] (+)= A[smem] * B[smem]; issued by a single thread.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+// D[tmem] (+)= A[smem] * B[smem] (tcgen05 kind::f16: bf16 or fp16 operands,
+// the type given by the instruction descriptor); issued by a single thread.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate)
 {
     asm volatile("{\n\t.reg .pred p;\n\t"
@@ -128,6 +174,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32])
         r[i] = __uint_as_float(u[i]);
 }
 
+// 8 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&r)[8])
+{
+    uint32_t u[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
+                 "tcgen05.wait::ld.sync.aligned;"
+                 : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]),
+                   "=r"(u[6]), "=r"(u[7])
+                 : "r"(taddr) : "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        r[i] = __uint_as_float(u[i]);
+}
+
 // ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
@@ -144,20 +204,81 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *mbar, uint32_t b
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
                  :: "r"(smem_u32(mbar)), "r"(bytes) : "memory");
 }
+// try_wait suspends the thread until the phase completes or about
+// kSuspendNs nanoseconds pass, so waiting threads leave the issue slots to the
+// others instead of polling.
+constexpr uint32_t kSuspendNs = 20000;
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *mbar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(smem_u32(mbar)), "r"(parity), "n"(kSuspendNs) : "memory");
+    return ok != 0;
+}
+
+// Non-blocking test of a phase (unlike try_wait it never suspends the thread).
+__device__ __forceinline__ bool mbar_test(uint64_t *mbar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
                  "selp.u32 %0, 1, 0, p;\n\t}"
                  : "=r"(ok) : "r"(smem_u32(mbar)), "r"(parity) : "memory");
     return ok != 0;
 }
 
-// Bounded wait: gives up after ~2^22 polls (each poll may itself suspend for
-// a short hardware-defined time), returning false.  Callers turn a false into
-// a device status bit and leave the kernel without touching more data.
-constexpr uint32_t kWaitPolls = 1u << 22;
+// Wait with cluster-scope acquire (pairs with remote release arrivals).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *mbar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(smem_u32(mbar)), "r"(parity), "n"(kSuspendNs) : "memory");
+    return ok != 0;
+}
+// Arrive, with cluster-scope release, on the mbarrier at the same offset in
+// the shared memory of CTA `rank` of this cluster.
+__device__ __forceinline__ void mbar_arrive_remote(uint64_t *local_mbar, uint32_t rank)
+{
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local_mbar)), "r"(rank));
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(remote) : "memory");
+}
+// Asynchronous 4-byte store into the shared memory of CTA `rank` of this
+// cluster, completing 4 transaction bytes on that CTA's mbarrier at the same
+// offset as `local_mbar` (no fence needed: the receiver waits on its barrier).
+__device__ __forceinline__ void st_async_remote(const void *local_dst, float v, uint64_t *local_mbar,
+                                                uint32_t rank)
+{
+    uint32_t rd, rb;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rd) : "r"(smem_u32(local_dst)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_u32(local_mbar)), "r"(rank));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+                 :: "r"(rd), "r"(__float_as_uint(v)), "r"(rb) : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Named CTA barriers: producers arrive without waiting, the consumer syncs.
+__device__ __forceinline__ void named_arrive(uint32_t id, uint32_t nthreads)
+{
+    asm volatile("bar.arrive %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads)
+{
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
+}
+
+// Bounded wait: gives up after kWaitPolls suspended polls (~2 s), returning
+// false.  Callers turn a false into a device status bit and leave the kernel
+// without touching more data.
+constexpr uint32_t kWaitPolls = 100000;
 __device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity)
 {
     for (uint32_t i = 0; i < kWaitPolls; ++i)
