@@ -6,7 +6,7 @@ the thin Python binding over that ABI (torch tensors -> device pointers) plus
 the build script and the seeded synthetic input generator.
 """
 from ._binding import (GdnError, alloc_workspace, check_device_status, decode, load, prefill,
-                       status_string, workspace_bytes)
+                       prefill_noalloc, status_string, workspace_bytes)
 
 __all__ = ["GdnError", "alloc_workspace", "check_device_status", "decode", "load", "prefill",
-           "status_string", "workspace_bytes"]
+           "prefill_noalloc", "status_string", "workspace_bytes"]

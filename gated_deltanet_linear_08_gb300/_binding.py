@@ -25,7 +25,7 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED",
                 3: "GDN_ERR_ALIGNMENT", 4: "GDN_ERR_CUDA", 5: "GDN_ERR_DEVICE_STATUS",
                 6: "GDN_ERR_WORKSPACE"}
 EXPORTED = ("gdn_status_string", "gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_decode",
-            "gdn_check_device_status")
+            "gdn_check_device_status", "gdn_prefill_noalloc")
 
 
 class GdnError(RuntimeError):
@@ -62,6 +62,9 @@ def load(path: Optional[str] = None):
             lib.gdn_decode.argtypes = [ctypes.POINTER(Shape), P, P, P, P, P, P, P, P, P, P, f32,
                                        P, P]
             lib.gdn_decode.restype = ctypes.c_int
+            lib.gdn_prefill_noalloc.argtypes = [ctypes.POINTER(Shape), P, P, P, P, P, P, P, P, P,
+                                                P, P, f32, P, P, P]
+            lib.gdn_prefill_noalloc.restype = ctypes.c_int
             lib.gdn_check_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
             lib.gdn_check_device_status.restype = ctypes.c_int
             _lib = lib
@@ -141,6 +144,33 @@ def prefill(q, k, v, a, b, A_log, dt_bias, cu_seqlens, init_state=None, z=None, 
         _ptr(norm_w, bf, "norm_w", dev), float(eps), _ptr(out, bf, "out", dev),
         _ptr(final_state, f32, "final_state", dev), _ptr(workspace, torch.uint8, "workspace", dev),
         int(workspace.numel()), _stream_handle(stream, dev))
+    _check(code)
+    return out, final_state
+
+
+def prefill_noalloc(q, k, v, a, b, A_log, dt_bias, cu_seqlens, init_state=None, z=None,
+                    norm_w=None, eps: float = 1e-6, out=None, final_state=None, stream=None):
+    """Prefill through ``gdn_prefill_noalloc``: the library's own fixed scratch
+    instead of a workspace, for callers that cannot allocate device memory.
+    ``out`` and ``final_state`` should be passed in by such callers (the
+    defaults here allocate them with torch for convenience)."""
+    dev = q.device
+    T, hk = q.shape[0], q.shape[1]
+    hv = v.shape[1]
+    N = cu_seqlens.shape[0] - 1
+    if out is None:
+        out = torch.empty(T, hv, 128, dtype=torch.bfloat16, device=dev)
+    if final_state is None:
+        final_state = torch.empty(N, hv, 128, 128, dtype=torch.float32, device=dev)
+    bf, f32 = torch.bfloat16, torch.float32
+    shape = make_shape(N, T, hk, hv)
+    code = load().gdn_prefill_noalloc(
+        ctypes.byref(shape), _ptr(q, bf, "q", dev), _ptr(k, bf, "k", dev), _ptr(v, bf, "v", dev),
+        _ptr(a, bf, "a", dev), _ptr(b, bf, "b", dev), _ptr(A_log, f32, "A_log", dev),
+        _ptr(dt_bias, f32, "dt_bias", dev), _ptr(init_state, f32, "init_state", dev),
+        _ptr(cu_seqlens, torch.int32, "cu_seqlens", dev), _ptr(z, bf, "z", dev),
+        _ptr(norm_w, bf, "norm_w", dev), float(eps), _ptr(out, bf, "out", dev),
+        _ptr(final_state, f32, "final_state", dev), _stream_handle(stream, dev))
     _check(code)
     return out, final_state
 

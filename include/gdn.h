@@ -101,6 +101,34 @@ gdn_status_t gdn_prefill(const gdn_shape_t *shape,
                          void *stream);
 
 /*
+ * gdn_prefill_noalloc -- the same prefill as gdn_prefill for callers that
+ * cannot allocate device memory: hosts that hand a kernel only their own
+ * pre-registered buffers and forbid device allocation once running (an
+ * allocation synchronises the device and can fragment a pool sized at
+ * start-up), or plain-C callers with no device allocator.  The paper has no
+ * counterpart for this entry point.
+ *
+ * Arguments and results are those of gdn_prefill without the workspace: the
+ * scratch lives in a fixed 64 MiB array of device memory that the library
+ * holds on every GPU that loads it, until the process exits (about 1,700
+ * packed tokens at Hk = 16, Hv = 32).  A shape whose
+ * gdn_prefill_workspace_bytes exceeds 64 MiB returns GDN_ERR_WORKSPACE
+ * before any launch.  Nothing in the array needs clearing between calls.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  Every
+ * call on a device shares the one array, so calls that may overlap on the
+ * GPU (on different streams, or from different host threads) race and must
+ * be ordered by the caller.  Allocates nothing.
+ */
+gdn_status_t gdn_prefill_noalloc(const gdn_shape_t *shape,
+                                 const void *q, const void *k, const void *v,
+                                 const void *a, const void *b,
+                                 const float *A_log, const float *dt_bias,
+                                 const float *init_state, const int32_t *cu_seqlens,
+                                 const void *z, const void *norm_w, float eps,
+                                 void *out, float *final_state, void *stream);
+
+/*
  * gdn_decode -- one token per sequence, the state updated in place (the
  * recurrent-state slots of serving, SGLang page "[Perf] Pack the Qwen3.5 GDN
  * input projection on CUDA", section Accuracy Tests: mamba slots).  Each
