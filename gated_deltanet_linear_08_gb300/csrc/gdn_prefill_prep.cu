@@ -12,7 +12,9 @@
 //   D_a  = [K; Q] K^T                       raw bf16 q/k (exact), tcgen05
 //   A_ij = beta_i e^{G_i-G_j} r_ki r_kj (K K^T)_ij      (j < i)
 //   P_ij = e^{G_i-G_j} r_qi r_kj (Q K^T)_ij             (j <= i)
-//   T    = (I + A)^{-1}                     fp32, blocked 16x16 substitution
+//   T    = (I + A)^{-1}                     16x16 diagonal blocks exactly in
+//                                           fp32, the blocks below them by
+//                                           warp-level fp16 products
 //   MT   = [I; P] T diag(beta)              tcgen05, fp16 operands
 //   [W; R] = MT diag(Gam) Kn                tcgen05, fp16 operands
 //   WQ   = [-W; diag(Gam r_q) Q - R]
@@ -26,6 +28,12 @@
 // fp16 operands (10-bit mantissa) keep the rounding of the state-side
 // products 8x below bf16's; the bf16 inputs convert exactly.  A value of v
 // outside the fp16 range sets the range status bit.
+//
+// The chunk's q, k and v tiles arrive by tensor-map copies issued at entry:
+// k and q land directly in the 128-byte-swizzled layout the first tcgen05
+// product reads, so no thread waits on a global load.
+#include <cuda.h>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tc05.cuh"
@@ -34,32 +42,47 @@ namespace gdn {
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kApad = 65;   // fp32 row stride of the A/T matrix (bank-conflict free)
 
-// Shared-memory map (offsets from a 1024-byte aligned base), ~51 KB so that
-// four CTAs share an SM.  Region R0 is reused as the kernel goes:
-//   [K;Q] bf16 image (until D_a completes)
-//   -> fp32 A/T [64][65], fp32 X [16][48], fp16 (T diag(beta))^T
-//   -> fp16 Kn image (after T diag(beta) has been consumed by the MT product)
-constexpr uint32_t kOffKQ = 0;          // bf16 [K;Q] raw, 2 halves x 128 rows x 128 B
-constexpr uint32_t kOffA = 0;           // fp32 A, then T, [64][65]
-constexpr uint32_t kOffX = 16640;       // fp32 X [16][48] of the blocked inverse
-constexpr uint32_t kOffTb = 20480;      // fp16 (T diag(beta))^T, 64 rows x 128 B
-constexpr uint32_t kOffKn = 0;          // fp16 Kn [token][dk], dk halves of 8 KB
-constexpr uint32_t kOffP = 32768;       // fp16 [I; P], 128 rows x 128 B; then A'
-constexpr uint32_t kOffSmall = 49152;   // per-row scalars, barrier, TMEM slot
-constexpr uint32_t kSmemBytes = kOffSmall + 2048 + 1024;  // + alignment slack
+// Shared-memory map (offsets from a 1024-byte aligned base), ~72 KB so that
+// three CTAs share an SM.
+//   KQ: bf16 [K;Q] as the 128-row A operand of D_a, dk halves 16 KB apart
+//       (K rows of half h at h*16K, Q rows at h*16K + 8K); after D_a the K
+//       rows are rescaled in place into the fp16 Kn operand.
+//   V : bf16 tile of v (dk halves of 8 KB); after its conversion the fp16
+//       [I; P] operand; after MT the fp16 A' = MT diag(Gam) operand.
+//   Tb: fp16 (T diag(beta))^T, B operand of MT.
+//   Ah, Th, Xs: 16x16 fp16 blocks for the inverse (512 B each): the six
+//       blocks of A below the diagonal blocks (row-major), the ten lower
+//       blocks of T stored transposed, one scratch block per merging warp.
+//   Ad: fp32 diagonal 16x16 blocks of A.
+constexpr uint32_t kOffKQ = 0;
+constexpr uint32_t kOffQ = 8192;        // + h * 16384
+constexpr uint32_t kOffV = 32768;
+constexpr uint32_t kOffP = 32768;
+constexpr uint32_t kOffTb = 49152;
+constexpr uint32_t kOffAh = 57344;
+constexpr uint32_t kOffTh = kOffAh + 6 * 512;
+constexpr uint32_t kOffXs = kOffTh + 10 * 512;
+constexpr uint32_t kOffAd = kOffXs + 3 * 512;
+constexpr uint32_t kOffSmall = kOffAd + 4 * 16 * 16 * 4;
+constexpr uint32_t kTmaBytes = 6 * 8192;   // k, q, v: two 64x64 bf16 boxes each
 
 // TMEM: D_a in [0,64), MT in [64,128); [W; R] reuses [0,128) once both have
 // been read.
 constexpr uint32_t kTmemCols = 128;
 
+constexpr float kLog2e = 1.4426950408889634f;
+
 struct Small {
-    float rk[64], rq[64], G[64], gam[64], beta[64];
-    uint64_t mbar;
+    float rk[64], rq[64];
+    float G2[64];      // in-chunk cumulative gate times log2(e)
+    float gam[64];     // e^{G_i}
+    float beta[64];
+    uint64_t mbar_tma, mbar_mma;
     uint32_t tmem_base;
     int fail;
 };
+constexpr uint32_t kSmemBytes = kOffSmall + ((sizeof(Small) + 127) / 128) * 128 + 1024;
 
 // Locate global chunk `gc`: first token and valid rows.  Returns false when gc
 // lies past the last chunk.  Malformed cu_seqlens (decreasing or outside
@@ -85,89 +108,85 @@ __device__ bool locate_chunk(const PrefillArgs &p, int gc, int &tok0, int &L, bo
     return false;
 }
 
-// Bounded wait on the CTA's MMA barrier; a timeout is recorded once and later
-// waits are skipped so the CTA runs to its end without hanging.
-__device__ __forceinline__ void wait_mma(Small *sm, uint32_t parity, uint32_t *status)
+// Bounded wait on one of the CTA's barriers; a timeout is recorded once and
+// later waits are skipped so the CTA runs to its end without hanging.
+__device__ __forceinline__ void wait_bar(Small *sm, uint64_t *bar, uint32_t parity, uint32_t *status)
 {
     if (*reinterpret_cast<volatile int *>(&sm->fail))
         return;
-    if (!mbar_wait(&sm->mbar, parity)) {
+    if (!mbar_wait(bar, parity)) {
         sm->fail = 1;
         set_status(status, kStatusWaitTimeout);
     }
 }
 
-// Inverse of the unit lower-triangular (I + A), in place in fp32 (row stride
-// kApad).  16x16 diagonal blocks by forward substitution (one thread per
-// column), then block rows a = 1..3: X = sum_c A_ac T_cb, T_ab = -T_aa X.
-template <int a>
-__device__ __forceinline__ void invert_block_row(float *A, float *X, int tid)
+// 16x16 fp16 block, 32-byte rows; the two 16-byte halves of row r swap places
+// when bit 2 of r is set, so the eight rows ldmatrix reads at once fall in
+// distinct banks.
+__device__ __forceinline__ uint32_t blk_off(int r, int half)
 {
-    constexpr int ncols = 16 * a;                    // columns 0 .. 16a-1
-    constexpr int per = 16 * ncols / kThreads;       // outputs per thread (2, 4, 6)
-    static_assert(16 * ncols % kThreads == 0, "outputs divide evenly");
-    // X[r][col] = sum over blocks b = col/16 .. a-1 of A[16a+r][16b..] T[16b..][col]
-#pragma unroll
-    for (int k = 0; k < per; ++k) {
-        const int e = tid + k * kThreads;
-        const int r = e / ncols, col = e % ncols, cb = col >> 4;
-        const float *arow = A + (16 * a + r) * kApad;
-        float acc = 0.f;
-#pragma unroll
-        for (int b = 0; b < a; ++b) {
-            if (b >= cb) {
-#pragma unroll
-                for (int m = 0; m < 16; ++m)
-                    acc = fmaf(arow[16 * b + m], A[(16 * b + m) * kApad + col], acc);
-            }
-        }
-        X[r * 48 + col] = acc;
-    }
-    __syncthreads();
-    // T[16a+r][col] = -sum_m T_aa[r][m] X[m][col]; T_aa's upper part is stored
-    // as zeros, so the sum runs over all 16 m
-#pragma unroll
-    for (int k = 0; k < per; ++k) {
-        const int e = tid + k * kThreads;
-        const int r = e / ncols, col = e % ncols;
-        const float *trow = A + (16 * a + r) * kApad + 16 * a;
-        float acc = 0.f;
-#pragma unroll
-        for (int m = 0; m < 16; ++m)
-            acc = fmaf(trow[m], X[m * 48 + col], acc);
-        A[(16 * a + r) * kApad + col] = -acc;
-    }
-    __syncthreads();
+    return (uint32_t)(r * 32 + ((half ^ ((r >> 2) & 1)) << 4));
+}
+__device__ __forceinline__ int ah_index(int a, int b) { return a * (a - 1) / 2 + b; }   // a > b
+__device__ __forceinline__ int th_index(int a, int b) { return a * (a + 1) / 2 + b; }   // a >= b
+// Row address lane t contributes to an x4 ldmatrix over one block.
+__device__ __forceinline__ uint32_t ldsm_addr(uint32_t blk, int lane)
+{
+    return blk + blk_off((lane & 7) + ((lane >> 3) & 1) * 8, lane >> 4);
+}
+// Byte offset of (row n, k index i) in the Tb image (64 rows of 64 fp16).
+__device__ __forceinline__ uint32_t tb_off(int n, int i)
+{
+    return (uint32_t)(n * 128 + ((((i >> 3) ^ n) & 7) << 4) + (i & 7) * 2);
 }
 
-__device__ void invert_unit_lower(float *A, float *X, int tid)
+// One block of T below the diagonal blocks, for warp-level products:
+//   X = sum_{c=b}^{a-1} A_ac T_cb,   T_ab = -T_aa X
+// written (transposed) into Th and, scaled by beta of its column, into Tb.
+__device__ void merge_block(unsigned char *sm, const Small *s, int a, int b, int lane, int warp)
 {
-    const int b = (tid >> 4) & 3, l = tid & 15, o = b * 16;
-    float x[16];
-    if (tid < 64) {
+    const uint32_t sbase = smem_u32(sm);
+    const int g = lane >> 2, t4 = lane & 3;
+    float x[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    for (int c = b; c < a; ++c) {
+        uint32_t fa[4], fb[4];
+        ldsm_x4(ldsm_addr(sbase + kOffAh + ah_index(a, c) * 512, lane), fa);   // A_ac, row-major
+        ldsm_x4(ldsm_addr(sbase + kOffTh + th_index(c, b) * 512, lane), fb);   // T_cb, stored as T^T
+        mma16816(x[0], fa[0], fa[1], fa[2], fa[3], fb[0], fb[2]);
+        mma16816(x[1], fa[0], fa[1], fa[2], fa[3], fb[1], fb[3]);
+    }
+    // X -> fp16 scratch, row-major [k][n]
+    unsigned char *xs = sm + kOffXs + warp * 512;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float acc = (i == l) ? 1.f : 0.f;
+    for (int j = 0; j < 2; ++j) {
+        *reinterpret_cast<uint32_t *>(xs + blk_off(g, j) + t4 * 4) = pack2h(x[j][0], x[j][1]);
+        *reinterpret_cast<uint32_t *>(xs + blk_off(g + 8, j) + t4 * 4) = pack2h(x[j][2], x[j][3]);
+    }
+    __syncwarp();
+    uint32_t fx[4], ft[4];
+    ldsm_x4_t(ldsm_addr(sbase + kOffXs + warp * 512, lane), fx);            // B = X
+    ldsm_x4_t(ldsm_addr(sbase + kOffTh + th_index(a, a) * 512, lane), ft);  // A = T_aa from T^T
+    float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    mma16816(d[0], ft[0], ft[2], ft[1], ft[3], fx[0], fx[1]);
+    mma16816(d[1], ft[0], ft[2], ft[1], ft[3], fx[2], fx[3]);
+    __half *th = reinterpret_cast<__half *>(sm + kOffTh + th_index(a, b) * 512);
 #pragma unroll
-            for (int j = 0; j < i; ++j)
-                acc = fmaf(-A[(o + i) * kApad + o + j], x[j], acc);
-            x[i] = (i < l) ? 0.f : acc;
+    for (int j = 0; j < 2; ++j) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int r = g + (e >> 1) * 8, cc = 8 * j + 2 * t4 + (e & 1);   // element (r, cc) of T_ab
+            const float v = -d[j][e];
+            th[(blk_off(cc, r >> 3) >> 1) + (r & 7)] = __float2half_rn(v);
+            *reinterpret_cast<__half *>(sm + kOffTb + tb_off(16 * b + cc, 16 * a + r)) =
+                __float2half_rn(v * s->beta[16 * b + cc]);
         }
     }
-    __syncthreads();   // every read of the diagonal blocks precedes the writes
-    if (tid < 64) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            A[(o + i) * kApad + o + l] = x[i];
-    }
-    __syncthreads();
-    invert_block_row<1>(A, X, tid);
-    invert_block_row<2>(A, X, tid);
-    invert_block_row<3>(A, X, tid);
 }
 
-__global__ void __launch_bounds__(kThreads, 4)
-prep_kernel(PrefillArgs p)
+
+__global__ void __launch_bounds__(kThreads, 3)
+prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+            const __grid_constant__ CUtensorMap tm_v)
 {
     const int gc = blockIdx.x, h = blockIdx.y;
     const int hv = p.hv, hk = p.hk, group = hv / hk, hq = h / group;
@@ -194,67 +213,26 @@ prep_kernel(PrefillArgs p)
     unsigned char *ws_k = p.workspace + (size_t)p.max_chunks * hv * kPerVHead
                           + ((size_t)gc * hk + hq) * kKBytes;
 
+    // ---- 1. tile copies of k, q (straight into the D_a operand layout) and v
     if (tid == 0) {
-        mbar_init(&s->mbar, 1);
+        mbar_init(&s->mbar_tma, 1);
+        mbar_init(&s->mbar_mma, 1);
         mbar_fence_init();
         s->fail = 0;
+        mbar_arrive_expect_tx(&s->mbar_tma, kTmaBytes);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            tma_load_3d(sm + kOffKQ + hf * 16384, &tm_k, hf * 64, hq, tok0, &s->mbar_tma);
+            tma_load_3d(sm + kOffQ + hf * 16384, &tm_q, hf * 64, hq, tok0, &s->mbar_tma);
+            tma_load_3d(sm + kOffV + hf * 8192, &tm_v, hf * 64, h, tok0, &s->mbar_tma);
+        }
     }
     if (warp == 0) {
         tmem_alloc(&s->tmem_base, kTmemCols);
         tmem_relinquish();
         tc_fence_before();
     }
-
-    // ---- 1. raw K, Q (rows 0-63 K, 64-127 Q) -> bf16 [K;Q] image and sums of
-    //         squares; V -> four fp16 [token][32] value-slice images in the
-    //         workspace.  16 threads per 256-byte row.
-    const __nv_bfloat16 *qg = reinterpret_cast<const __nv_bfloat16 *>(p.q);
-    const __nv_bfloat16 *kg = reinterpret_cast<const __nv_bfloat16 *>(p.k);
-    const __nv_bfloat16 *vg = reinterpret_cast<const __nv_bfloat16 *>(p.v);
-    {
-        const int chunk = tid & 15;
-        for (int m = 0; m < 16; ++m) {
-            const int r = (tid >> 4) + 8 * m;      // 0..127
-            const int i = r & 63;
-            uint4 u = make_uint4(0, 0, 0, 0);
-            if (i < L) {
-                const __nv_bfloat16 *src = (r < 64 ? kg : qg) + ((size_t)(tok0 + i) * hk + hq) * kD;
-                u = *reinterpret_cast<const uint4 *>(src + chunk * 8);
-            }
-            float f[8];
-            unpack8(u, f);
-            float ss = 0.f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                ss = fmaf(f[e], f[e], ss);
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1)
-                ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            if (chunk == 0) {
-                const float rn = (i < L) ? 1.f / sqrtf(ss + kL2Eps) : 0.f;
-                if (r < 64) s->rk[i] = rn; else s->rq[i] = rn;
-            }
-            *reinterpret_cast<uint4 *>(sm + kOffKQ + (chunk >> 3) * 16384
-                                       + sw128_chunk_offset(r, chunk & 7)) = u;
-        }
-        bool over = false;
-        for (int m = 0; m < 8; ++m) {
-            const int i = (tid >> 4) + 8 * m;      // token 0..63
-            uint4 u = make_uint4(0, 0, 0, 0);
-            if (i < L)
-                u = *reinterpret_cast<const uint4 *>(vg + ((size_t)(tok0 + i) * hv + h) * kD + chunk * 8);
-            float f[8];
-            unpack8(u, f);
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                over |= !(fabsf(f[e]) <= kHalfMax);
-            // value columns 8*chunk..+7 sit in slice chunk/4, 16-byte chunk chunk%4
-            *reinterpret_cast<uint4 *>(ws_vimg + (chunk >> 2) * 4096 + sw64_chunk_offset(i, chunk & 3)) = pack8h(f);
-        }
-        if (over)
-            set_status(p.status, kStatusRange);
-    }
-    // ---- 2. gates: g, beta, in-chunk inclusive cumsum G
+    // ---- 2. gates: g, beta, in-chunk inclusive cumsum G (under the copies)
     if (tid < 64) {
         float gv = 0.f, bv = 0.f;
         if (tid < L) {
@@ -268,13 +246,54 @@ prep_kernel(PrefillArgs p)
             const float t = __shfl_up_sync(0xffffffffu, c, o);
             if (lane >= o) c += t;
         }
-        s->G[tid] = c;
+        s->G2[tid] = c;
         s->beta[tid] = bv;
     }
-    fence_async_smem();
     __syncthreads();
-    if (tid >= 32 && tid < 64)
-        s->G[tid] += s->G[31];
+    float Gnat = 0.f;
+    if (tid < 64)
+        Gnat = s->G2[tid] + (tid >= 32 ? s->G2[31] : 0.f);
+    __syncthreads();
+    if (tid < 64) {
+        s->G2[tid] = Gnat * kLog2e;
+        s->gam[tid] = expf(Gnat);
+    }
+    wait_bar(s, &s->mbar_tma, 0, p.status);
+
+    // rows past the chunk's end hold the next sequence's tokens (or the
+    // copy's zero fill): clear them in all six tiles
+    if (L < kC) {
+        const int nr = kC - L;
+        for (int e = tid; e < 6 * nr * 8; e += kThreads) {
+            const int tile = e / (nr * 8), rem = e - tile * nr * 8;
+            const uint32_t base = tile < 4 ? (uint32_t)((tile >> 1) * 16384 + (tile & 1) * 8192)
+                                           : kOffV + (uint32_t)(tile - 4) * 8192;
+            *reinterpret_cast<uint4 *>(sm + base + (L + (rem >> 3)) * 128 + (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        __syncthreads();
+    }
+    // inverse L2 norms: thread t takes row t of [K; Q]
+    {
+        const int i = tid & 63;
+        const uint32_t rb = (tid < 64 ? 0u : 8192u) + (uint32_t)i * 128u;
+        float ss = 0.f;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                float f[8];
+                unpack8(*reinterpret_cast<const uint4 *>(sm + hf * 16384 + rb + c * 16), f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    ss = fmaf(f[e], f[e], ss);
+            }
+        }
+        const float rn = (i < L) ? 1.f / sqrtf(ss + kL2Eps) : 0.f;
+        if (tid < 64) s->rk[i] = rn; else s->rq[i] = rn;
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
     if (warp == 0) {
         // D_a = [K;Q] K^T in bf16: the B operand is the K rows of the same image
         tc_fence_after();
@@ -286,46 +305,86 @@ prep_kernel(PrefillArgs p)
                 const uint32_t off = kOffKQ + (kk >> 2) * 16384 + (kk & 3) * 32;
                 mma_f16(d, make_sw128_desc(sbase + off), make_sw128_desc(sbase + off), idesc, kk > 0);
             }
-            mma_commit(&s->mbar);
+            mma_commit(&s->mbar_mma);
         }
         __syncwarp();
     }
-    __syncthreads();   // G complete before gam
-    if (tid < 64)
-        s->gam[tid] = expf(s->G[tid]);
-    wait_mma(s, 0, p.status);
-    tc_fence_after();
 
-    // ---- 3. A (fp32, rows 0-63) and P (fp16, rows 64-127 of [I; P]); A
-    //         overwrites the [K;Q] image, which D_a has finished reading.
-    //         Columns are taken 32 at a time to bound register use.
-    float *sA = reinterpret_cast<float *>(sm + kOffA);
-    float *sX = reinterpret_cast<float *>(sm + kOffX);
+    // ---- 3. v -> four fp16 [token][32] value-slice images in the workspace
+    {
+        bool over = false;
+        for (int e = tid; e < 1024; e += kThreads) {
+            const int i = e >> 4, c16 = e & 15;
+            float f[8];
+            unpack8(*reinterpret_cast<const uint4 *>(sm + kOffV + (c16 >> 3) * 8192 + sw128_chunk_offset(i, c16 & 7)), f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                over |= !(fabsf(f[j]) <= kHalfMax);
+            // value columns 8*c16..+7 sit in slice c16/4, 16-byte chunk c16%4
+            *reinterpret_cast<uint4 *>(ws_vimg + (c16 >> 2) * 4096 + sw64_chunk_offset(i, c16 & 3)) = pack8h(f);
+        }
+        if (over)
+            set_status(p.status, kStatusRange);
+    }
+    wait_bar(s, &s->mbar_mma, 0, p.status);
+    tc_fence_after();
+    // Kn = diag(r_k) K in fp16, in place of the K rows (the operand layout of
+    // [W; R] below and of the scan kernel's state update)
+    for (int e = tid; e < 1024; e += kThreads) {
+        const int hf = e >> 9, i = (e >> 3) & 63, c = e & 7;
+        const uint32_t off = sw128_chunk_offset(i, c);
+        uint4 *ptr = reinterpret_cast<uint4 *>(sm + kOffKQ + hf * 16384 + off);
+        float f[8];
+        unpack8(*ptr, f);
+        const float rk = s->rk[i];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] *= rk;
+        const uint4 hv8 = pack8h(f);
+        *ptr = hv8;
+        if (h % group == 0)
+            *reinterpret_cast<uint4 *>(ws_k + hf * 8192 + off) = hv8;
+    }
+    __syncthreads();   // the v tile is consumed before [I; P] overwrites it
+
+    // ---- 4. A (fp16 blocks below the diagonal, fp32 diagonal blocks) from
+    //         rows 0-63 and P (fp16, rows 64-127 of [I; P]) from rows 64-127.
+    //         Rows 0-31 of A and of P need only columns 0-31.
     {
         const uint32_t ta = s->tmem_base + ((uint32_t)(warp * 32) << 16);
-        const int i = tid & 63;
-        const float Gi = s->G[i];
+        const int i = tid & 63, a = i >> 4;
+        const float G2i = s->G2[i];
         const float ci = (tid < 64) ? s->beta[i] * s->rk[i] : s->rq[i];
+        float *Ad = reinterpret_cast<float *>(sm + kOffAd);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
+            if (half == 1 && !(warp & 1)) {
+                if (warp == 2) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<uint4 *>(sm + kOffP + sw128_chunk_offset(64 + i, 4 + c)) = make_uint4(0, 0, 0, 0);
+                }
+                continue;
+            }
             float d[32];
             tmem_ld32(ta + half * 32, d);
-            if (tid < 64) {
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int j = half * 32 + jj;
-                    sA[i * kApad + j] = (j < i) ? ci * __expf(Gi - s->G[j]) * s->rk[j] * d[jj] : 0.f;
+            for (int c = 0; c < 4; ++c) {
+                const int j0 = half * 32 + c * 8, b = j0 >> 4;
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int j = j0 + e;
+                    const bool keep = (tid < 64) ? (j < i) : (j <= i);
+                    v[e] = keep ? ci * exp2f(G2i - s->G2[j]) * s->rk[j] * d[c * 8 + e] : 0.f;
                 }
-            } else {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float pv[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int j = half * 32 + c * 8 + e;
-                        pv[e] = (j <= i) ? ci * __expf(Gi - s->G[j]) * s->rk[j] * d[c * 8 + e] : 0.f;
-                    }
-                    *reinterpret_cast<uint4 *>(sm + kOffP + sw128_chunk_offset(64 + i, half * 4 + c)) = pack8h(pv);
+                if (tid >= 64) {
+                    *reinterpret_cast<uint4 *>(sm + kOffP + sw128_chunk_offset(64 + i, half * 4 + c)) = pack8h(v);
+                } else if (b < a) {
+                    *reinterpret_cast<uint4 *>(sm + kOffAh + ah_index(a, b) * 512 + blk_off(i & 15, (j0 >> 3) & 1)) = pack8h(v);
+                } else if (b == a) {
+                    float4 *dst = reinterpret_cast<float4 *>(Ad + a * 256 + (i & 15) * 16 + (j0 & 15));
+                    dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+                    dst[1] = make_float4(v[4], v[5], v[6], v[7]);
                 }
             }
         }
@@ -341,26 +400,58 @@ prep_kernel(PrefillArgs p)
     }
     __syncthreads();
 
-    // ---- 4. T = (I + A)^{-1} in fp32, then (T diag(beta))^T in fp16
-    invert_unit_lower(sA, sX, tid);
-    {
-        const int l = tid & 63, jh = tid >> 6;
-        const float bl = s->beta[l];
+    // ---- 5. T = (I + A)^{-1}: diagonal blocks by forward substitution in
+    //         fp32 (one thread per column), the upper blocks of Tb cleared
+    //         meanwhile, then the blocks below the diagonal by three rounds of
+    //         warp-level products (block distance 1, 2, 3)
+    if (tid < 64) {
+        const int b = tid >> 4, l = tid & 15;
+        const float *Ad = reinterpret_cast<const float *>(sm + kOffAd) + b * 256;
+        float x[16];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-            const int c = jh * 4 + cc;
-            float v[8];
+        for (int r = 0; r < 16; ++r) {
+            float acc = (r == l) ? 1.f : 0.f;
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                v[e] = sA[(c * 8 + e) * kApad + l] * bl;
-            *reinterpret_cast<uint4 *>(sm + kOffTb + sw128_chunk_offset(l, c)) = pack8h(v);
+            for (int j = 0; j < r; ++j)
+                acc = fmaf(-Ad[r * 16 + j], x[j], acc);
+            x[r] = (r < l) ? 0.f : acc;
+        }
+        // column l of T_bb: row l of the transposed block in Th, row 16b+l of Tb
+        unsigned char *th = sm + kOffTh + th_index(b, b) * 512;
+        const float bl = s->beta[16 * b + l];
+        const int n = 16 * b + l;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            float v[8], w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                v[e] = x[8 * q + e];
+                w[e] = x[8 * q + e] * bl;
+            }
+            *reinterpret_cast<uint4 *>(th + blk_off(l, q)) = pack8h(v);
+            *reinterpret_cast<uint4 *>(sm + kOffTb + n * 128 + ((((2 * b + q) ^ n) & 7) << 4)) = pack8h(w);
+        }
+    } else {
+        for (int e = tid - 64; e < 64 * 8; e += 64) {
+            const int n = e >> 3, k8 = e & 7;
+            if (k8 < 2 * (n >> 4))
+                *reinterpret_cast<uint4 *>(sm + kOffTb + n * 128 + (((k8 ^ n) & 7) << 4)) = make_uint4(0, 0, 0, 0);
         }
     }
+    __syncthreads();
+    if (warp < 3)
+        merge_block(sm, s, warp + 1, warp, lane, warp);
+    __syncthreads();
+    if (warp < 2)
+        merge_block(sm, s, warp + 2, warp, lane, warp);
+    __syncthreads();
+    if (warp == 0)
+        merge_block(sm, s, 3, 0, lane, warp);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
 
-    // ---- 5. MT = [I; P] T diag(beta)   (fp32 in TMEM columns 64..127)
+    // ---- 6. MT = [I; P] T diag(beta)   (fp32 in TMEM columns 64..127)
     if (warp == 0) {
         tc_fence_after();
         if (lane == 0) {
@@ -370,36 +461,21 @@ prep_kernel(PrefillArgs p)
             for (int kk = 0; kk < 4; ++kk)
                 mma_f16(d, make_sw128_desc(sbase + kOffP + kk * 32),
                         make_sw128_desc(sbase + kOffTb + kk * 32), idesc, kk != 0);
-            mma_commit(&s->mbar);
+            mma_commit(&s->mbar_mma);
         }
         __syncwarp();
     }
-    // Kn = diag(r_k) K in fp16, [token][dk] in dk halves of 8 KB (the operand
-    // layout of [W; R] below and of the scan kernel's state update), built
-    // from a second read of K while the MMA runs; it overwrites A, which is
-    // no longer needed (T diag(beta) lives elsewhere)
-    for (int e = tid; e < 1024; e += kThreads) {
-        const int half = e >> 9, i = (e >> 3) & 63, cc = e & 7;
-        float f[8];
-        if (i < L) {
-            unpack8(*reinterpret_cast<const uint4 *>(kg + ((size_t)(tok0 + i) * hk + hq) * kD + half * 64 + cc * 8), f);
-            const float rk = s->rk[i];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) f[j] *= rk;
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) f[j] = 0.f;
-        }
-        const uint4 hv8 = pack8h(f);
-        const uint32_t off = sw128_chunk_offset(i, cc);
-        *reinterpret_cast<uint4 *>(sm + kOffKn + half * 8192 + off) = hv8;
-        if (h % group == 0)
-            *reinterpret_cast<uint4 *>(ws_k + half * 8192 + off) = hv8;
+    // row scales for the state update while the MMA runs
+    if (tid < 64) {
+        const float Gl = s->G2[63];
+        ws_scal[tid] = (tid < L) ? exp2f(Gl - s->G2[tid]) : 0.f;
+        if (tid == 0)
+            ws_scal[64] = exp2f(Gl);
     }
-    wait_mma(s, 1, p.status);
+    wait_bar(s, &s->mbar_mma, 1, p.status);
     tc_fence_after();
 
-    // ---- 6. MT row t -> workspace (fp16 image); A' = MT diag(Gam) -> smem
+    // ---- 7. MT row t -> workspace (fp16 image); A' = MT diag(Gam) -> smem
     //         (A' reuses the [I; P] buffer: the MMA that read it has completed)
     {
         const uint32_t ta = s->tmem_base + ((uint32_t)(warp * 32) << 16) + 64;
@@ -424,8 +500,8 @@ prep_kernel(PrefillArgs p)
     tc_fence_before();
     __syncthreads();
 
-    // ---- 7. [W; R] = A' Kn into TMEM columns 0..127 (D_a and MT have been
-    //         read).  B = Kn read MN-major: dk halves 8 KB apart, 8-token
+    // ---- 8. [W; R] = A' Kn into TMEM columns 0..127 (D_a and MT have been
+    //         read).  B = Kn read MN-major: dk halves 16 KB apart, 8-token
     //         groups 1024 bytes apart; N = 128 key dims.
     if (warp == 0) {
         tc_fence_after();
@@ -435,22 +511,16 @@ prep_kernel(PrefillArgs p)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
                 mma_f16(d, make_sw128_desc(sbase + kOffP + kk * 32),
-                        make_desc(sbase + kOffKn + kk * 2048, 8192, 1024, kSw128), idesc, kk != 0);
-            mma_commit(&s->mbar);
+                        make_desc(sbase + kOffKQ + kk * 2048, 16384, 1024, kSw128), idesc, kk != 0);
+            mma_commit(&s->mbar_mma);
         }
         __syncwarp();
     }
-    // row scales for the state update while the MMA runs
-    if (tid < 64) {
-        const float Gl = s->G[63];
-        ws_scal[tid] = (tid < L) ? expf(Gl - s->G[tid]) : 0.f;
-        if (tid == 0)
-            ws_scal[64] = expf(Gl);
-    }
-    wait_mma(s, 0, p.status);
+    wait_bar(s, &s->mbar_mma, 0, p.status);
     tc_fence_after();
 
-    // ---- 8. WQ = [-W; diag(Gam r_q) Q - R] -> workspace (two 64-wide halves)
+    // ---- 9. WQ = [-W; diag(Gam r_q) Q - R] -> workspace (two 64-wide halves);
+    //         q comes from the tile still held in shared memory
     {
         const int i = tid - 64;   // token row of the Q part (warps 2-3)
         const float qs = (tid >= 64) ? s->gam[i] * s->rq[i] : 0.f;
@@ -459,17 +529,20 @@ prep_kernel(PrefillArgs p)
             tmem_ld32(s->tmem_base + ((uint32_t)(warp * 32) << 16) + gq * 32, dv);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                float qv[8];
-                if (tid >= 64 && i < L)
-                    unpack8(reinterpret_cast<const uint4 *>(qg + ((size_t)(tok0 + i) * hk + hq) * kD + gq * 32)[u], qv);
-                else
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) qv[e] = 0.f;
-                float w8[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    w8[e] = (tid < 64) ? -dv[u * 8 + e] : fmaf(qs, qv[e], -dv[u * 8 + e]);
                 const int col = gq * 32 + u * 8;   // 0..127
+                float w8[8];
+                if (tid >= 64) {
+                    float qv[8];
+                    unpack8(*reinterpret_cast<const uint4 *>(
+                                sm + kOffQ + (col >> 6) * 16384 + sw128_chunk_offset(i, (col & 63) >> 3)), qv);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        w8[e] = fmaf(qs, qv[e], -dv[u * 8 + e]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        w8[e] = -dv[u * 8 + e];
+                }
                 *reinterpret_cast<uint4 *>(ws_wq + (col >> 6) * 16384 + sw128_chunk_offset(tid, (col & 63) >> 3)) = pack8h(w8);
             }
         }
@@ -484,6 +557,40 @@ prep_kernel(PrefillArgs p)
     }
 }
 
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up once through the runtime.
+EncodeTiledFn encode_fn()
+{
+    static const EncodeTiledFn fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess
+            || q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+// Tensor map over a bf16 [T][heads][128] tensor: boxes of 64 tokens x 64
+// dims of one head, 128-byte swizzled in shared memory, zero fill past T.
+bool encode_tile_map(CUtensorMap *map, const void *base, int heads, int tokens)
+{
+    const EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    const cuuint64_t dims[3] = {128, (cuuint64_t)heads, (cuuint64_t)tokens};
+    const cuuint64_t strides[2] = {256, (cuuint64_t)heads * 256};
+    const cuuint32_t box[3] = {64, 1, 64};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 cudaError_t launch_prefill_prep(const PrefillArgs &p, cudaStream_t stream)
@@ -495,8 +602,12 @@ cudaError_t launch_prefill_prep(const PrefillArgs &p, cudaStream_t stream)
             return e;
         configured = true;
     }
+    CUtensorMap tq, tk, tv;
+    if (!encode_tile_map(&tq, p.q, p.hk, p.total_tokens) || !encode_tile_map(&tk, p.k, p.hk, p.total_tokens)
+        || !encode_tile_map(&tv, p.v, p.hv, p.total_tokens))
+        return cudaErrorInvalidValue;
     dim3 grid(p.max_chunks, p.hv);
-    prep_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
+    prep_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p, tq, tk, tv);
     return cudaGetLastError();
 }
 
