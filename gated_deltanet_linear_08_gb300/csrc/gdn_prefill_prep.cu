@@ -8,7 +8,7 @@
 //
 // Per chunk (L <= 64 valid rows; padded rows are zero and change nothing),
 // with r_k, r_q the inverse L2 norms, g/beta the gate and beta, G the in-chunk
-// cumulative gate, Gam_i = e^{G_i}, Kn = diag(r_k) K:
+// cumulative gate, Gam_i = e^{G_i}, eps_i = e^{G_last - G_i}, Kn = diag(r_k) K:
 //   D_a  = [K; Q] K^T                       raw bf16 q/k (exact), tcgen05
 //   A_ij = beta_i e^{G_i-G_j} r_ki r_kj (K K^T)_ij      (j < i)
 //   P_ij = e^{G_i-G_j} r_qi r_kj (Q K^T)_ij             (j <= i)
@@ -16,18 +16,20 @@
 //                                           fp32, the blocks below them by
 //                                           warp-level fp16 products
 //   MT   = [I; P] T diag(beta)              tcgen05, fp16 operands
-//   [W; R] = MT diag(Gam) Kn                tcgen05, fp16 operands
-//   WQ   = [-W; diag(Gam r_q) Q - R]
-// and it writes, as the fp16 swizzled byte images the scan kernel copies
-// straight into shared memory: WQ (128x128), MT (128x64), V (four [token][32]
-// value slices), Kn ([token][dk], once per key head) and the row scales
-// e^{G_last - G_i} and e^{G_last}.
-// With U = T diag(beta) V - W S0 the chunk's outputs are
-//   scale (P T diag(beta) V + (diag(Gam) Qn - P W) S0) = scale [MT V + WQ S0]_bottom
-// and U = [MT V + WQ S0]_top, so the serial scan needs one accumulator.
-// fp16 operands (10-bit mantissa) keep the rounding of the state-side
-// products 8x below bf16's; the bf16 inputs convert exactly.  A value of v
-// outside the fp16 range sets the range status bit.
+//   [W; R] = MT diag(Gam) Kn                tcgen05
+//   Ec   = Kn^T diag(eps) T diag(beta)      tcgen05 (A = Kn read MN-major)
+//   Mc   = -Kn^T diag(eps) W                tcgen05
+// Within the chunk the delta rule gives U = T diag(beta) V - W S0 (the
+// UT/WY form), S1 = e^{G_last} S0 + Kn^T diag(eps) U and outputs
+// scale (diag(Gam) Qn S0 + P U), so
+//   S1 = e^{G_last} S0 + Mc S0 + Ec V
+//   o  = scale (Qc S0 + Fc V),  Qc = diag(Gam r_q) Q - R,  Fc = P T diag(beta)
+// and the serial scan needs one tensor-core product per chunk on its chain.
+// Everything is written as the fp16 swizzled byte images the scan kernel
+// copies straight into shared memory (layout in kernels.h).  fp16 operands
+// (10-bit mantissa) keep the rounding of the state-side products 8x below
+// bf16's; the bf16 inputs convert exactly.  A value of v outside the fp16
+// range sets the range status bit.
 //
 // The chunk's q, k and v tiles arrive by tensor-map copies issued at entry:
 // k and q land directly in the 128-byte-swizzled layout the first tcgen05
@@ -41,10 +43,10 @@
 namespace gdn {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
 
-// Shared-memory map (offsets from a 1024-byte aligned base), ~72 KB so that
-// three CTAs share an SM.
+// Shared-memory map (offsets from a 1024-byte aligned base), ~100 KB so that
+// two CTAs share an SM.
 //   KQ: bf16 [K;Q] as the 128-row A operand of D_a, dk halves 16 KB apart
 //       (K rows of half h at h*16K, Q rows at h*16K + 8K); after D_a the K
 //       rows are rescaled in place into the fp16 Kn operand.
@@ -55,6 +57,9 @@ constexpr int kThreads = 128;
 //       blocks of A below the diagonal blocks (row-major), the ten lower
 //       blocks of T stored transposed, one scratch block per merging warp.
 //   Ad: fp32 diagonal 16x16 blocks of A.
+//   BE: fp16 diag(eps) T diag(beta) [token][64], MN-major B operand of Ec.
+//   BM: fp16 -diag(eps) W [token][dk], MN-major B operand of Mc, dk halves
+//       8 KB apart.
 constexpr uint32_t kOffKQ = 0;
 constexpr uint32_t kOffQ = 8192;        // + h * 16384
 constexpr uint32_t kOffV = 32768;
@@ -64,12 +69,14 @@ constexpr uint32_t kOffAh = 57344;
 constexpr uint32_t kOffTh = kOffAh + 6 * 512;
 constexpr uint32_t kOffXs = kOffTh + 10 * 512;
 constexpr uint32_t kOffAd = kOffXs + 3 * 512;
-constexpr uint32_t kOffSmall = kOffAd + 4 * 16 * 16 * 4;
+constexpr uint32_t kOffBE = 73728;
+constexpr uint32_t kOffBM = kOffBE + 8192;
+constexpr uint32_t kOffSmall = kOffBM + 16384;
 constexpr uint32_t kTmaBytes = 6 * 8192;   // k, q, v: two 64x64 bf16 boxes each
 
-// TMEM: D_a in [0,64), MT in [64,128); [W; R] reuses [0,128) once both have
-// been read.
-constexpr uint32_t kTmemCols = 128;
+// TMEM: D_a in [0,64), MT in [64,128); then Ec in [0,64) and [W; R] in
+// [128,256); then Mc in [0,128).
+constexpr uint32_t kTmemCols = 256;
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -78,6 +85,7 @@ struct Small {
     float G2[64];      // in-chunk cumulative gate times log2(e)
     float gam[64];     // e^{G_i}
     float beta[64];
+    float eps[64];     // e^{G_last - G_i}, 0 past the chunk's end
     uint64_t mbar_tma, mbar_mma;
     uint32_t tmem_base;
     int fail;
@@ -184,13 +192,17 @@ __device__ void merge_block(unsigned char *sm, const Small *s, int a, int b, int
 }
 
 
-__global__ void __launch_bounds__(kThreads, 3)
+
+__global__ void __launch_bounds__(kThreads, 2)
 prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v)
 {
     const int gc = blockIdx.x, h = blockIdx.y;
-    const int hv = p.hv, hk = p.hk, group = hv / hk, hq = h / group;
+    const int hv = p.hv, hq = h / (hv / p.hk);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // warp w reads TMEM lane quadrant q = w % 4 and column half ch = w / 4
+    const int q = warp & 3, ch = warp >> 2;
+    const int row = 32 * q + lane;          // TMEM lane of this thread
 
     int tok0 = 0, L = 0;
     bool bad = false;
@@ -205,13 +217,7 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Small *s = reinterpret_cast<Small *>(sm + kOffSmall);
     const uint32_t sbase = smem_u32(sm);
-
-    unsigned char *ws_wq = p.workspace + ((size_t)gc * hv + h) * kPerVHead;
-    unsigned char *ws_mt = ws_wq + kWQBytes;
-    unsigned char *ws_vimg = ws_mt + kMTBytes;
-    float *ws_scal = reinterpret_cast<float *>(ws_vimg + kVBytes);
-    unsigned char *ws_k = p.workspace + (size_t)p.max_chunks * hv * kPerVHead
-                          + ((size_t)gc * hk + hq) * kKBytes;
+    unsigned char *ws = p.workspace + ((size_t)gc * hv + h) * kPerVHead;
 
     // ---- 1. tile copies of k, q (straight into the D_a operand layout) and v
     if (tid == 0) {
@@ -258,6 +264,11 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
         s->G2[tid] = Gnat * kLog2e;
         s->gam[tid] = expf(Gnat);
     }
+    __syncthreads();
+    if (tid < 64)
+        s->eps[tid] = (tid < L) ? exp2f(s->G2[63] - s->G2[tid]) : 0.f;
+    if (tid == 0)
+        *reinterpret_cast<float4 *>(ws + kWsScal) = make_float4(exp2f(s->G2[63]), 0.f, 0.f, 0.f);
     wait_bar(s, &s->mbar_tma, 0, p.status);
 
     // rows past the chunk's end hold the next sequence's tokens (or the
@@ -272,24 +283,24 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
         }
         __syncthreads();
     }
-    // inverse L2 norms: thread t takes row t of [K; Q]
+    // inverse L2 norms: threads 2r, 2r+1 sum the two dk halves of row r of [K; Q]
     {
-        const int i = tid & 63;
-        const uint32_t rb = (tid < 64 ? 0u : 8192u) + (uint32_t)i * 128u;
+        const int r = tid >> 1, hf = tid & 1, i = r & 63;
+        const uint32_t rb = (uint32_t)hf * 16384u + (r < 64 ? 0u : 8192u) + (uint32_t)i * 128u;
         float ss = 0.f;
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
+        for (int c = 0; c < 8; ++c) {
+            float f[8];
+            unpack8(*reinterpret_cast<const uint4 *>(sm + rb + c * 16), f);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                float f[8];
-                unpack8(*reinterpret_cast<const uint4 *>(sm + hf * 16384 + rb + c * 16), f);
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    ss = fmaf(f[e], f[e], ss);
-            }
+            for (int e = 0; e < 8; ++e)
+                ss = fmaf(f[e], f[e], ss);
         }
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
         const float rn = (i < L) ? 1.f / sqrtf(ss + kL2Eps) : 0.f;
-        if (tid < 64) s->rk[i] = rn; else s->rq[i] = rn;
+        if (hf == 0) {
+            if (r < 64) s->rk[i] = rn; else s->rq[i] = rn;
+        }
     }
     fence_async_smem();
     tc_fence_before();
@@ -313,7 +324,9 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
     // ---- 3. v -> four fp16 [token][32] value-slice images in the workspace
     {
         bool over = false;
-        for (int e = tid; e < 1024; e += kThreads) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int e = tid + k * kThreads;
             const int i = e >> 4, c16 = e & 15;
             float f[8];
             unpack8(*reinterpret_cast<const uint4 *>(sm + kOffV + (c16 >> 3) * 8192 + sw128_chunk_offset(i, c16 & 7)), f);
@@ -321,64 +334,59 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
             for (int j = 0; j < 8; ++j)
                 over |= !(fabsf(f[j]) <= kHalfMax);
             // value columns 8*c16..+7 sit in slice c16/4, 16-byte chunk c16%4
-            *reinterpret_cast<uint4 *>(ws_vimg + (c16 >> 2) * 4096 + sw64_chunk_offset(i, c16 & 3)) = pack8h(f);
+            *reinterpret_cast<uint4 *>(ws + kWsV + (c16 >> 2) * 4096 + sw64_chunk_offset(i, c16 & 3)) = pack8h(f);
         }
         if (over)
             set_status(p.status, kStatusRange);
     }
     wait_bar(s, &s->mbar_mma, 0, p.status);
     tc_fence_after();
-    // Kn = diag(r_k) K in fp16, in place of the K rows (the operand layout of
-    // [W; R] below and of the scan kernel's state update)
-    for (int e = tid; e < 1024; e += kThreads) {
+    // Kn = diag(r_k) K in fp16, in place of the K rows (the operand of the
+    // [W; R], Ec and Mc products)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int e = tid + k * kThreads;
         const int hf = e >> 9, i = (e >> 3) & 63, c = e & 7;
-        const uint32_t off = sw128_chunk_offset(i, c);
-        uint4 *ptr = reinterpret_cast<uint4 *>(sm + kOffKQ + hf * 16384 + off);
+        uint4 *ptr = reinterpret_cast<uint4 *>(sm + kOffKQ + hf * 16384 + sw128_chunk_offset(i, c));
         float f[8];
         unpack8(*ptr, f);
         const float rk = s->rk[i];
 #pragma unroll
         for (int j = 0; j < 8; ++j) f[j] *= rk;
-        const uint4 hv8 = pack8h(f);
-        *ptr = hv8;
-        if (h % group == 0)
-            *reinterpret_cast<uint4 *>(ws_k + hf * 8192 + off) = hv8;
+        *ptr = pack8h(f);
     }
     __syncthreads();   // the v tile is consumed before [I; P] overwrites it
 
     // ---- 4. A (fp16 blocks below the diagonal, fp32 diagonal blocks) from
-    //         rows 0-63 and P (fp16, rows 64-127 of [I; P]) from rows 64-127.
-    //         Rows 0-31 of A and of P need only columns 0-31.
+    //         lanes 0-63 and P (fp16, rows 64-127 of [I; P]) from lanes
+    //         64-127, columns 32 ch .. 32 ch + 31.  Rows 0-31 of A and of P
+    //         have nothing at columns 32-63.
     {
-        const uint32_t ta = s->tmem_base + ((uint32_t)(warp * 32) << 16);
-        const int i = tid & 63, a = i >> 4;
-        const float G2i = s->G2[i];
-        const float ci = (tid < 64) ? s->beta[i] * s->rk[i] : s->rq[i];
-        float *Ad = reinterpret_cast<float *>(sm + kOffAd);
+        const int i = row & 63, a = i >> 4;
+        if (ch == 1 && (q & 1) == 0) {
+            if (q == 2) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            if (half == 1 && !(warp & 1)) {
-                if (warp == 2) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        *reinterpret_cast<uint4 *>(sm + kOffP + sw128_chunk_offset(64 + i, 4 + c)) = make_uint4(0, 0, 0, 0);
-                }
-                continue;
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<uint4 *>(sm + kOffP + sw128_chunk_offset(64 + i, 4 + c)) = make_uint4(0, 0, 0, 0);
             }
+        } else {
+            const float G2i = s->G2[i];
+            const float ci = (q < 2) ? s->beta[i] * s->rk[i] : s->rq[i];
+            float *Ad = reinterpret_cast<float *>(sm + kOffAd);
             float d[32];
-            tmem_ld32(ta + half * 32, d);
+            tmem_ld32(s->tmem_base + ((uint32_t)(32 * q) << 16) + ch * 32, d);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const int j0 = half * 32 + c * 8, b = j0 >> 4;
+                const int j0 = ch * 32 + c * 8, b = j0 >> 4;
                 float v[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int j = j0 + e;
-                    const bool keep = (tid < 64) ? (j < i) : (j <= i);
+                    const bool keep = (q < 2) ? (j < i) : (j <= i);
                     v[e] = keep ? ci * exp2f(G2i - s->G2[j]) * s->rk[j] * d[c * 8 + e] : 0.f;
                 }
-                if (tid >= 64) {
-                    *reinterpret_cast<uint4 *>(sm + kOffP + sw128_chunk_offset(64 + i, half * 4 + c)) = pack8h(v);
+                if (q >= 2) {
+                    *reinterpret_cast<uint4 *>(sm + kOffP + sw128_chunk_offset(64 + i, ch * 4 + c)) = pack8h(v);
                 } else if (b < a) {
                     *reinterpret_cast<uint4 *>(sm + kOffAh + ah_index(a, b) * 512 + blk_off(i & 15, (j0 >> 3) & 1)) = pack8h(v);
                 } else if (b == a) {
@@ -392,9 +400,9 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 uint32_t w[4] = {0, 0, 0, 0};
-                if ((i >> 3) == c)
-                    w[(i & 7) >> 1] = (i & 1) ? 0x3C000000u : 0x00003C00u;   // fp16 1.0
-                *reinterpret_cast<uint4 *>(sm + kOffP + sw128_chunk_offset(i, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+                if ((tid >> 3) == c)
+                    w[(tid & 7) >> 1] = (tid & 1) ? 0x3C000000u : 0x00003C00u;   // fp16 1.0
+                *reinterpret_cast<uint4 *>(sm + kOffP + sw128_chunk_offset(tid, c)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
         }
     }
@@ -421,18 +429,18 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
         const float bl = s->beta[16 * b + l];
         const int n = 16 * b + l;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
+        for (int qq = 0; qq < 2; ++qq) {
             float v[8], w[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                v[e] = x[8 * q + e];
-                w[e] = x[8 * q + e] * bl;
+                v[e] = x[8 * qq + e];
+                w[e] = x[8 * qq + e] * bl;
             }
-            *reinterpret_cast<uint4 *>(th + blk_off(l, q)) = pack8h(v);
-            *reinterpret_cast<uint4 *>(sm + kOffTb + n * 128 + ((((2 * b + q) ^ n) & 7) << 4)) = pack8h(w);
+            *reinterpret_cast<uint4 *>(th + blk_off(l, qq)) = pack8h(v);
+            *reinterpret_cast<uint4 *>(sm + kOffTb + n * 128 + ((((2 * b + qq) ^ n) & 7) << 4)) = pack8h(w);
         }
     } else {
-        for (int e = tid - 64; e < 64 * 8; e += 64) {
+        for (int e = tid - 64; e < 64 * 8; e += kThreads - 64) {
             const int n = e >> 3, k8 = e & 7;
             if (k8 < 2 * (n >> 4))
                 *reinterpret_cast<uint4 *>(sm + kOffTb + n * 128 + (((k8 ^ n) & 7) << 4)) = make_uint4(0, 0, 0, 0);
@@ -465,34 +473,33 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
         }
         __syncwarp();
     }
-    // row scales for the state update while the MMA runs
-    if (tid < 64) {
-        const float Gl = s->G2[63];
-        ws_scal[tid] = (tid < L) ? exp2f(Gl - s->G2[tid]) : 0.f;
-        if (tid == 0)
-            ws_scal[64] = exp2f(Gl);
-    }
     wait_bar(s, &s->mbar_mma, 1, p.status);
     tc_fence_after();
 
-    // ---- 7. MT row t -> workspace (fp16 image); A' = MT diag(Gam) -> smem
-    //         (A' reuses the [I; P] buffer: the MMA that read it has completed)
+    // ---- 7. MT (row = lane, columns 32 ch ..) -> A' = MT diag(Gam) for
+    //         [W; R]; rows 64-127 are Fc; rows 0-63 scaled by eps form BE.
+    //         A' reuses the [I; P] buffer: the MMA that read it has completed.
     {
-        const uint32_t ta = s->tmem_base + ((uint32_t)(warp * 32) << 16) + 64;
+        float mrow[32];
+        tmem_ld32(s->tmem_base + ((uint32_t)(32 * q) << 16) + 64 + ch * 32, mrow);
+        const int i = row & 63;
+        const float ei = (q < 2) ? s->eps[i] : 0.f;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            float mrow[32];
-            tmem_ld32(ta + half * 32, mrow);
+        for (int c = 0; c < 4; ++c) {
+            float m8[8], a8[8];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float m8[8], a8[8];
+            for (int e = 0; e < 8; ++e) {
+                m8[e] = mrow[c * 8 + e];
+                a8[e] = m8[e] * s->gam[ch * 32 + c * 8 + e];
+            }
+            const uint32_t off = sw128_chunk_offset(i, ch * 4 + c);
+            *reinterpret_cast<uint4 *>(sm + kOffP + sw128_chunk_offset(row, ch * 4 + c)) = pack8h(a8);
+            if (q >= 2) {
+                *reinterpret_cast<uint4 *>(ws + kWsFc + off) = pack8h(m8);
+            } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    m8[e] = mrow[c * 8 + e];
-                    a8[e] = m8[e] * s->gam[half * 32 + c * 8 + e];
-                }
-                *reinterpret_cast<uint4 *>(ws_mt + sw128_chunk_offset(tid, half * 4 + c)) = pack8h(m8);
-                *reinterpret_cast<uint4 *>(sm + kOffP + sw128_chunk_offset(tid, half * 4 + c)) = pack8h(a8);
+                for (int e = 0; e < 8; ++e) m8[e] *= ei;
+                *reinterpret_cast<uint4 *>(sm + kOffBE + off) = pack8h(m8);
             }
         }
     }
@@ -500,18 +507,22 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
     tc_fence_before();
     __syncthreads();
 
-    // ---- 8. [W; R] = A' Kn into TMEM columns 0..127 (D_a and MT have been
-    //         read).  B = Kn read MN-major: dk halves 16 KB apart, 8-token
-    //         groups 1024 bytes apart; N = 128 key dims.
+    // ---- 8. Ec = Kn^T BE (TMEM [0,64); A = Kn read MN-major: dk halves 16 KB
+    //         apart, 16-token steps of 2 KB) and [W; R] = A' Kn (TMEM
+    //         [128,256); B = Kn read MN-major)
     if (warp == 0) {
         tc_fence_after();
         if (lane == 0) {
-            const uint32_t d = s->tmem_base;
-            constexpr uint32_t idesc = make_idesc_f16(128, 128, false, true);
+            constexpr uint32_t idesc_e = make_idesc_f16(128, 64, true, true);
+            constexpr uint32_t idesc_w = make_idesc_f16(128, 128, false, true);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-                mma_f16(d, make_sw128_desc(sbase + kOffP + kk * 32),
-                        make_desc(sbase + kOffKQ + kk * 2048, 16384, 1024, kSw128), idesc, kk != 0);
+                mma_f16(s->tmem_base, make_desc(sbase + kOffKQ + kk * 2048, 16384, 1024, kSw128),
+                        make_desc(sbase + kOffBE + kk * 2048, 8192, 1024, kSw128), idesc_e, kk != 0);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_f16(s->tmem_base + 128, make_sw128_desc(sbase + kOffP + kk * 32),
+                        make_desc(sbase + kOffKQ + kk * 2048, 16384, 1024, kSw128), idesc_w, kk != 0);
             mma_commit(&s->mbar_mma);
         }
         __syncwarp();
@@ -519,32 +530,76 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
     wait_bar(s, &s->mbar_mma, 0, p.status);
     tc_fence_after();
 
-    // ---- 9. WQ = [-W; diag(Gam r_q) Q - R] -> workspace (two 64-wide halves);
-    //         q comes from the tile still held in shared memory
+    // ---- 9. rows 0-63 of [W; R] -> BM = -diag(eps) W; rows 64-127 ->
+    //         Qc = diag(Gam r_q) Q - R (q from the tile still in shared
+    //         memory); every lane's Ec row -> workspace.  Columns: dk half ch.
     {
-        const int i = tid - 64;   // token row of the Q part (warps 2-3)
-        const float qs = (tid >= 64) ? s->gam[i] * s->rq[i] : 0.f;
-        for (int gq = 0; gq < 4; ++gq) {
+        const int i = row & 63;
+        const float ei = s->eps[i];
+        const float qs = (q >= 2) ? s->gam[i] * s->rq[i] : 0.f;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
             float dv[32];
-            tmem_ld32(s->tmem_base + ((uint32_t)(warp * 32) << 16) + gq * 32, dv);
+            tmem_ld32(s->tmem_base + ((uint32_t)(32 * q) << 16) + 128 + ch * 64 + g * 32, dv);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int col = gq * 32 + u * 8;   // 0..127
+                const int c = g * 4 + u;   // 16-byte chunk within the dk half
                 float w8[8];
-                if (tid >= 64) {
+                if (q >= 2) {
                     float qv[8];
-                    unpack8(*reinterpret_cast<const uint4 *>(
-                                sm + kOffQ + (col >> 6) * 16384 + sw128_chunk_offset(i, (col & 63) >> 3)), qv);
+                    unpack8(*reinterpret_cast<const uint4 *>(sm + kOffQ + ch * 16384 + sw128_chunk_offset(i, c)), qv);
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         w8[e] = fmaf(qs, qv[e], -dv[u * 8 + e]);
+                    *reinterpret_cast<uint4 *>(ws + (ch ? kWsQc1 : kWsQc0) + sw128_chunk_offset(i, c)) = pack8h(w8);
                 } else {
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
-                        w8[e] = -dv[u * 8 + e];
+                        w8[e] = -ei * dv[u * 8 + e];
+                    *reinterpret_cast<uint4 *>(sm + kOffBM + ch * 8192 + sw128_chunk_offset(i, c)) = pack8h(w8);
                 }
-                *reinterpret_cast<uint4 *>(ws_wq + (col >> 6) * 16384 + sw128_chunk_offset(tid, (col & 63) >> 3)) = pack8h(w8);
             }
+        }
+        float ev[32];
+        tmem_ld32(s->tmem_base + ((uint32_t)(32 * q) << 16) + ch * 32, ev);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float e8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) e8[e] = ev[c * 8 + e];
+            *reinterpret_cast<uint4 *>(ws + kWsEc + sw128_chunk_offset(row, ch * 4 + c)) = pack8h(e8);
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- 10. Mc = Kn^T BM into TMEM [0,128) (Ec has been read)
+    if (warp == 0) {
+        tc_fence_after();
+        if (lane == 0) {
+            constexpr uint32_t idesc = make_idesc_f16(128, 128, true, true);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_f16(s->tmem_base, make_desc(sbase + kOffKQ + kk * 2048, 16384, 1024, kSw128),
+                        make_desc(sbase + kOffBM + kk * 2048, 8192, 1024, kSw128), idesc, kk != 0);
+            mma_commit(&s->mbar_mma);
+        }
+        __syncwarp();
+    }
+    wait_bar(s, &s->mbar_mma, 1, p.status);
+    tc_fence_after();
+    // Mc row = lane (output dk), columns = input dk half ch
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+        float mv[32];
+        tmem_ld32(s->tmem_base + ((uint32_t)(32 * q) << 16) + ch * 64 + g * 32, mv);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            float m8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) m8[e] = mv[u * 8 + e];
+            *reinterpret_cast<uint4 *>(ws + (ch ? kWsMc1 : kWsMc0) + sw128_chunk_offset(row, g * 4 + u)) = pack8h(m8);
         }
     }
 

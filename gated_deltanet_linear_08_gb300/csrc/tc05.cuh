@@ -174,6 +174,22 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32])
         r[i] = __uint_as_float(u[i]);
 }
 
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&r)[16])
+{
+    uint32_t u[16];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+                 "tcgen05.wait::ld.sync.aligned;"
+                 : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]),
+                   "=r"(u[6]), "=r"(u[7]), "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]),
+                   "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
+                 : "r"(taddr) : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        r[i] = __uint_as_float(u[i]);
+}
+
 // 8 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&r)[8])
 {
@@ -216,6 +232,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *mbar, uint32_t parity)
                  "selp.u32 %0, 1, 0, p;\n\t}"
                  : "=r"(ok) : "r"(smem_u32(mbar)), "r"(parity), "n"(kSuspendNs) : "memory");
     return ok != 0;
+}
+
+// Plain arrive (release, CTA scope) on a local mbarrier.
+__device__ __forceinline__ void mbar_arrive(uint64_t *mbar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(mbar)) : "memory");
 }
 
 // Non-blocking test of a phase (unlike try_wait it never suspends the thread).
