@@ -41,7 +41,7 @@ METRIC = "GDN prefill tokens/s & decode GB/s at Hv=32,D=128; % of tensor/HBM roo
 PREFILL_FLOP_PER_TOKEN_HEAD = 10 * 64 * 128 + 6 * 128 * 128   # 180,224 (C=64 chunked count)
 N_ROTATE = 8
 KERNEL_SOURCES = ["gdn_api.cu", "gdn_decode.cu", "gdn_prefill_prep.cu", "gdn_prefill_scan.cu",
-                  "common.cuh", "tc05.cuh", "kernels.h"]
+                  "gdn_prefill_out.cu", "common.cuh", "tc05.cuh", "kernels.h"]
 
 
 def load_peaks():
@@ -424,7 +424,7 @@ def main():
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16"],
                      "unit": "TFLOP/s", "frac": tflops / peaks["bf16"],
                      "traffic": ncu_traffic("prefill"),
-                     "kernel": "gdn_prefill call (prep + scan kernels)",
+                     "kernel": "gdn_prefill call (prep, scan and output kernels)",
                      "peak_kind": f"{peaks['src']} bf16 burst",
                      "work": f"{flops} algorithmic flop per call "
                              f"({PREFILL_FLOP_PER_TOKEN_HEAD} per token per value head)"},
@@ -441,7 +441,7 @@ def main():
                                 "kernel": "decode_kernel",
                                 "peak_kind": f"{peaks['src']} HBM copy",
                                 "work": f"{dbytes} algorithmic bytes per call"}},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 4 * args.steps,
         "clocks": clk.summary(),
     }
     if not args.no_e2e:

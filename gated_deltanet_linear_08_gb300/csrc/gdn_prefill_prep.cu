@@ -25,8 +25,8 @@
 //   S1 = e^{G_last} S0 + Mc S0 + Ec V
 //   o  = scale (Qc S0 + Fc V),  Qc = diag(Gam r_q) Q - R,  Fc = P T diag(beta)
 // and the serial scan needs one tensor-core product per chunk on its chain.
-// Everything is written as the fp16 swizzled byte images the scan kernel
-// copies straight into shared memory (layout in kernels.h).  fp16 operands
+// Everything is written as the fp16 swizzled byte images the scan and output
+// kernels copy straight into shared memory (layout in kernels.h).  fp16 operands
 // (10-bit mantissa) keep the rounding of the state-side products 8x below
 // bf16's; the bf16 inputs convert exactly.  A value of v outside the fp16
 // range sets the range status bit.

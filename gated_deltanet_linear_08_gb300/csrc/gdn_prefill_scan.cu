@@ -1,94 +1,67 @@
 // gdn_prefill_scan.cu -- serial half of the chunked GDN prefill: the fp32
-// inter-chunk state scan, the chunk outputs and the optional gated RMSNorm
-// epilogue (JevAny page "Add opt-in fused Qwen3.5 inference kernels",
-// Summary: chunked kernel followed by a fused gated RMSNorm; pegainfer page
-// "feat(qwen35): add SM120 FlashInfer GDN prefill candidate", Correctness:
-// chunked vs unchunked prefill, initial/final states).
+// inter-chunk state scan (JevAny page "Add opt-in fused Qwen3.5 inference
+// kernels", Summary: chunked kernel; pegainfer page "feat(qwen35): add SM120
+// FlashInfer GDN prefill candidate", Correctness: chunked vs unchunked
+// prefill, initial/final states).
 //
 // One CTA per (sequence, value head, 32-column slice of Dv).  The recurrence
 // is independent per value column, so the four slices of a head run in
-// parallel; with the epilogue on, the four CTAs of a head form a cluster and
-// exchange per-row sums of squares through distributed shared memory.
+// parallel with no communication.
 //
 // The prep kernel turns each chunk into an affine map of the state (tcgen05,
 // M = 128, fp16 operands; S is the fp32 slice, 128 x 32):
-//   S'  = e^{G_last} S + [Mc | Ec] [S; V]     one MMA chain, the only serial step
-//   o   = scale [Qc | Fc] [S; V]              off the chain
-// Ec V does not depend on S and is issued ahead, so the chain per chunk is
-// S (fp16 operand) -> 8 MMAs -> TMEM -> S' in registers.  Qc and Fc are
-// staged so that a 128-row operand starting 8 KB before them has them as
-// rows 64-127: the outputs land in TMEM lanes 64-127.
+//   S' = e^{G_last} S + [Mc | Ec] [S; V]
+// Ec V does not depend on S and is issued ahead, so the serial chain per
+// chunk is S (fp16 operand) -> 8 MMAs -> TMEM -> S' in registers.  Each
+// chunk's fp16 S operand is also copied to the workspace, where the output
+// kernel, fully parallel over chunks, turns it into the chunk's outputs.
 //
-// Roles (16 warps):
+// Roles (10 warps):
 //   warps 0-7   state: warp w holds TMEM lane quadrant w % 4 = state rows
 //               32 (w % 4) .. +31 and value columns 16 (w / 4) .. +15
-//   warp 8      issues every MMA
-//   warp 9      issues every bulk copy (two stages of 77 KB)
-//   warps 10, 11, 14, 15
-//               outputs: lane quadrants 2-3 = chunk rows 0-63, value
-//               columns 16 ((w - 10) / 4) .. +15; scale, gated RMSNorm and
-//               the stores, never on the state chain
-//   warps 12, 13 idle
-// With the epilogue on, each CTA sums its row partials over its 32 columns
-// and pushes them into every cluster CTA's receive buffer with asynchronous
-// remote stores that complete bytes on the receiver's mbarrier: no
-// cluster-scope fence, no cluster-wide barrier per chunk.
+//   warp 8      issues every MMA and the copies of S to the workspace
+//   warp 9      issues the operand copies (three stages of 52 KB)
 #include "common.cuh"
 #include "kernels.h"
 #include "tc05.cuh"
 
 namespace gdn {
 
-cudaError_t launch_prefill_prep(const PrefillArgs &p, cudaStream_t stream);
 
 namespace {
 
-constexpr int kThreads = 16 * 32;
+constexpr int kThreads = 10 * 32;
 constexpr int kStateWarps = 8;
 constexpr int kIssuerWarp = 8;
 constexpr int kLoaderWarp = 9;
-__device__ __forceinline__ bool is_output_warp(int w) { return w == 10 || w == 11 || w == 14 || w == 15; }
-// Named barriers (id, participating threads): producers arrive, consumers sync.
+// Named barrier (id, participating threads): state warps arrive, the issuer syncs.
 constexpr uint32_t kBarS = 1, kCntS = kStateWarps * 32 + 32;   // S operand written
-constexpr uint32_t kBarRed = 2, kCntRed = 4 * 32;               // output warps' row partials
 constexpr int kNv = 32;                 // value columns per CTA
 constexpr int kTiles = kD / kNv;        // 4 CTAs per (sequence, head)
 constexpr int kCols = 16;               // value columns per thread
 
-// Stage: the chunk's operand record (Mc, Qc, Ec, Fc as laid out in the
-// workspace) and this CTA's V slice.
-constexpr uint32_t kStV = (uint32_t)kOpsBytes;
-constexpr uint32_t kStageBytes = (uint32_t)kOpsBytes + 5120;
-constexpr int kStages = 2;
-constexpr uint32_t kLoadBytes = (uint32_t)kOpsBytes + 4096;
-constexpr uint32_t kOpsPiece = (uint32_t)kOpsBytes / 3;   // copied in three pieces
+// Stage: the chunk's Mc and Ec (one contiguous run of the record) and this
+// CTA's V slice.
+constexpr uint32_t kStEc = (uint32_t)kWsEc;
+constexpr uint32_t kStV = 49152;
+constexpr uint32_t kStageBytes = 53248;
+constexpr int kStages = 3;
+constexpr uint32_t kLoadBytes = 49152 + 4096;
 
 constexpr uint32_t kOffS = kStages * kStageBytes;   // two S operands [dk][32] fp16, MN-major, 8 KB each
 constexpr uint32_t kOffSmall = kOffS + 16384;
 
-// TMEM columns: chain accumulators at 0 / 32, output accumulators at 64 / 96.
-constexpr uint32_t kTmemCols = 128;
-constexpr uint32_t kColS = 0, kColO = 64;
-
-constexpr float kScale = 0.088388347648318440550f;  // 1/sqrt(128)
+// TMEM columns: chain accumulators at 0 / 32.
+constexpr uint32_t kTmemCols = 64;
 
 struct Small {
-    float red_local[2][2][64];  // output-row partial sums of squares [parity][column group][row]
-    float red_in[2][4][64];     // this CTA's row sums as received from [parity][cluster rank][row]
-    float w[kNv];               // gated-norm weight slice
     uint64_t full[kStages];     // stage landed (one arrival + bytes)
     uint64_t sfree[kStages];    // every MMA reading the stage has completed
-    uint64_t ofree[2];          // output accumulator read by the four output warps
     uint64_t bar_chain;
-    uint64_t bar_out[2];        // one per output accumulator, so it never runs two phases ahead
-    uint64_t red_full[2];       // all cluster CTAs' row sums received (1 arrival + 1 KB)
     uint32_t tmem_base;
     int fail;
 };
 constexpr uint32_t kSmemBytes = kOffSmall + ((sizeof(Small) + 127) / 128) * 128 + 1024;
-
-__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ bool failed(Small *s) { return *reinterpret_cast<volatile int *>(&s->fail) != 0; }
 
@@ -102,18 +75,6 @@ __device__ __forceinline__ bool wait_bar(Small *s, uint64_t *bar, uint32_t parit
         return false;
     }
     return true;
-}
-
-__device__ __forceinline__ bool wait_bar_cluster(Small *s, uint64_t *bar, uint32_t parity, uint32_t *status)
-{
-    if (failed(s))
-        return false;
-    for (uint32_t i = 0; i < kWaitPolls; ++i)
-        if (mbar_try_wait_cluster(bar, parity))
-            return true;
-    s->fail = 1;
-    set_status(status, kStatusWaitTimeout);
-    return false;
 }
 
 // Chunks that precede sequence n, with the same treatment of malformed
@@ -139,29 +100,38 @@ __device__ int chunk_base_of(const PrefillArgs &p, int n, int &tok0, int &len)
 
 // Descriptors of the stage operands (shared-memory byte address `st`).
 __device__ __forceinline__ uint64_t desc_k128(uint32_t addr) { return make_desc(addr, 16, 1024, kSw128); }
-__device__ __forceinline__ uint64_t desc_v(uint32_t st) { return make_desc(st + kStV, 512, 512, kSw64); }
 
-// D += X V (X = Ec, or Fc read as rows 64-127 of an operand starting 8 KB
-// earlier): four K steps over the chunk's 64 tokens.
-__device__ __forceinline__ void issue_xv(uint32_t d, uint32_t a_addr, uint32_t st, uint32_t idesc, bool acc)
+// D = Ec V: four K steps over the chunk's 64 tokens.
+__device__ __forceinline__ void issue_ecv(uint32_t d, uint32_t st, uint32_t idesc)
 {
-    const uint64_t a = desc_k128(a_addr), b = desc_v(st);
+    const uint64_t a = desc_k128(st + kStEc), b = make_desc(st + kStV, 512, 512, kSw64);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
-        mma_f16(d, a + (uint64_t)(kk * 2), b + (uint64_t)(kk * 64), idesc, (acc || kk != 0) ? 1u : 0u);
+        mma_f16(d, a + (uint64_t)(kk * 2), b + (uint64_t)(kk * 64), idesc, kk != 0 ? 1u : 0u);
 }
-// D += X S over the two 64-wide K halves of the state (X = Mc, or Qc as rows
-// 64-127 of operands starting 8 KB before each of its halves).
-__device__ __forceinline__ void issue_xs(uint32_t d, uint32_t a_lo, uint32_t a_hi, uint64_t ds, uint32_t idesc)
+// D += Mc S over the two 64-wide K halves of the state.
+__device__ __forceinline__ void issue_mcs(uint32_t d, uint32_t st, uint64_t ds, uint32_t idesc)
 {
-    const uint64_t a0 = desc_k128(a_lo), a1 = desc_k128(a_hi);
+    const uint64_t a0 = desc_k128(st + (uint32_t)kWsMc0), a1 = desc_k128(st + (uint32_t)kWsMc1);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
         mma_f16(d, (kk < 4 ? a0 : a1) + (uint64_t)((kk & 3) * 2), ds + (uint64_t)(kk * 64), idesc, 1u);
 }
 
+// Bulk shared -> global copy in the issuing thread's bulk group.
+__device__ __forceinline__ void bulk_s2g(void *dst_gmem, const void *src_smem, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 :: "l"(dst_gmem), "r"(smem_u32(src_smem)), "r"(bytes) : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" :: "n"(N) : "memory");
+}
 
-template <bool kNorm>
 __global__ void __launch_bounds__(kThreads, 1)
 scan_kernel(PrefillArgs p)
 {
@@ -185,18 +155,10 @@ scan_kernel(PrefillArgs p)
             mbar_init(&s->full[i], 1);
             mbar_init(&s->sfree[i], 1);
         }
-        mbar_init(&s->ofree[0], 4);
-        mbar_init(&s->ofree[1], 4);
         mbar_init(&s->bar_chain, 1);
-        mbar_init(&s->bar_out[0], 1);
-        mbar_init(&s->bar_out[1], 1);
-        mbar_init(&s->red_full[0], 1);
-        mbar_init(&s->red_full[1], 1);
         mbar_fence_init();
         s->fail = 0;
     }
-    if (kNorm && tid < kNv)
-        s->w[tid] = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.norm_w)[r * kNv + tid]);
     if (warp == 0) {
         tmem_alloc(&s->tmem_base, kTmemCols);
         tmem_relinquish();
@@ -204,10 +166,6 @@ scan_kernel(PrefillArgs p)
     }
     __syncthreads();
     tc_fence_after();
-    if (kNorm) {   // every CTA of the cluster is running before any DSMEM access
-        cluster_arrive();
-        cluster_wait();
-    }
     const uint32_t tbase = s->tmem_base;
     const uint32_t idesc = make_idesc_f16(128, kNv, false, true);
 
@@ -215,60 +173,57 @@ scan_kernel(PrefillArgs p)
         // ------------------------------------------------------------ issuer
         bool pre = false;   // Ec V of the current chunk already issued
         for (int c = 0; c < nck; ++c) {
-            const int b = c & 1;   // stage = S operand = accumulator buffer
-            const uint32_t st = sbase + b * kStageBytes;
-            const uint32_t dS = tbase + kColS + b * kNv, dO = tbase + kColO + b * kNv;
-            const uint64_t ds = make_desc(sbase + kOffS + b * 8192, 512, 512, kSw64);
-            if (lane == 0 && !pre && wait_bar(s, &s->full[b], (uint32_t)(c >> 1) & 1, p.status)) {
+            const int b = c & 1, st = c % kStages;   // S operand and accumulator buffer; stage
+            const uint32_t sst = sbase + st * kStageBytes;
+            const uint32_t dS = tbase + b * kNv;
+            if (lane == 0 && !pre && wait_bar(s, &s->full[st], (uint32_t)(c / kStages) & 1, p.status)) {
                 tc_fence_after();
-                issue_xv(dS, st + (uint32_t)kWsEc, st, idesc, false);
+                issue_ecv(dS, sst, idesc);
             }
             __syncwarp();
             named_sync(kBarS, kCntS);            // S(c) operand written
             if (lane == 0) {
+                // the S(c) operand -> workspace, for the output kernel; the copy
+                // of S(c-1) must have finished reading its buffer before the
+                // state warps (released by this chunk's chain) overwrite it
+                bulk_s2g(record(c) + kWsS + r * 8192, sm + kOffS + b * 8192, 8192);
+                bulk_wait_read<1>();
                 if (!failed(s)) {
                     tc_fence_after();
-                    issue_xs(dS, st + (uint32_t)kWsMc0, st + (uint32_t)kWsMc1, ds, idesc);
+                    issue_mcs(dS, sst, make_desc(sbase + kOffS + b * 8192, 512, 512, kSw64), idesc);
                 }
                 mma_commit(&s->bar_chain);
-                // outputs into an accumulator the output warps have finished reading
-                if (c < 2 || wait_bar(s, &s->ofree[b], ((uint32_t)(c >> 1) & 1) ^ 1, p.status)) {
-                    if (!failed(s)) {
-                        tc_fence_after();
-                        issue_xv(dO, st + (uint32_t)kWsFc - 8192, st, idesc, false);
-                        issue_xs(dO, st + (uint32_t)kWsQc0 - 8192, st + (uint32_t)kWsQc1 - 8192, ds, idesc);
-                    }
-                }
-                mma_commit(&s->bar_out[b]);
-                mma_commit(&s->sfree[b]);
+                mma_commit(&s->sfree[st]);
                 pre = false;
-                if (c + 1 < nck && !failed(s) && mbar_test(&s->full[b ^ 1], (uint32_t)((c + 1) >> 1) & 1)) {
+                const int ns = (c + 1) % kStages;
+                if (c + 1 < nck && !failed(s) && mbar_test(&s->full[ns], (uint32_t)((c + 1) / kStages) & 1)) {
                     tc_fence_after();
-                    issue_xv(tbase + kColS + (b ^ 1) * kNv, sbase + (b ^ 1) * kStageBytes + (uint32_t)kWsEc,
-                             sbase + (b ^ 1) * kStageBytes, idesc, false);
+                    issue_ecv(tbase + (b ^ 1) * kNv, sbase + ns * kStageBytes, idesc);
                     pre = true;
                 }
             }
             __syncwarp();
         }
+        if (lane == 0)
+            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");   // every S copy complete before exit
+        __syncwarp();
     } else if (warp == kLoaderWarp) {
         // ------------------------------------------------------------ loader
-        int issued[kStages] = {0, 0};
+        int issued[kStages] = {0, 0, 0};
         if (lane == 0) {
             for (int c = 0; c < nck; ++c) {
-                const int b = c & 1;
-                // chunk c goes into the stage chunk c-2 used, once every MMA
+                const int st = c % kStages;
+                // chunk c goes into the stage chunk c-3 used, once every MMA
                 // that read it has completed
-                if (c >= 2 && !wait_bar(s, &s->sfree[b], ((uint32_t)(c >> 1) & 1) ^ 1, p.status))
+                if (c >= kStages && !wait_bar(s, &s->sfree[st], (uint32_t)(c / kStages - 1) & 1, p.status))
                     break;
-                unsigned char *stage = sm + b * kStageBytes;
+                unsigned char *stage = sm + st * kStageBytes;
                 const unsigned char *rec = record(c);
-                mbar_arrive_expect_tx(&s->full[b], kLoadBytes);
-#pragma unroll
-                for (int k = 0; k < 3; ++k)
-                    bulk_g2s(stage + k * kOpsPiece, rec + k * kOpsPiece, kOpsPiece, &s->full[b]);
-                bulk_g2s(stage + kStV, rec + kWsV + r * 4096, 4096, &s->full[b]);
-                ++issued[b];
+                mbar_arrive_expect_tx(&s->full[st], kLoadBytes);
+                bulk_g2s(stage, rec, 24576, &s->full[st]);
+                bulk_g2s(stage + 24576, rec + 24576, 24576, &s->full[st]);
+                bulk_g2s(stage + kStV, rec + kWsV + r * 4096, 4096, &s->full[st]);
+                ++issued[st];
             }
             // no copy may still be landing in shared memory when the CTA exits
             if (failed(s)) {
@@ -278,11 +233,11 @@ scan_kernel(PrefillArgs p)
             }
         }
         __syncwarp();
-    } else if (warp < kStateWarps) {
+    } else {
         // ------------------------------------------------------------ state
         const int q = warp & 3, cg = warp >> 2;
         const int row = 32 * q + lane;     // TMEM lane = state row (dk)
-        const uint32_t tlane = tbase + ((uint32_t)(32 * q) << 16) + kColS + cg * kCols;
+        const uint32_t tlane = tbase + ((uint32_t)(32 * q) << 16) + cg * kCols;
         const size_t sidx = (((size_t)n * hv + h) * kD + row) * kD + r * kNv + cg * kCols;
         float S[kCols];
         if (p.init_state) {
@@ -331,79 +286,8 @@ scan_kernel(PrefillArgs p)
 #pragma unroll
         for (int j = 0; j < kCols / 4; ++j)
             reinterpret_cast<float4 *>(p.final_state + sidx)[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
-    } else if (is_output_warp(warp)) {
-        // ------------------------------------------------------------ outputs
-        const int q = warp & 3, cg = (warp - 10) >> 2;
-        const int orow = 32 * (q - 2) + lane;   // chunk row (TMEM lane 64 + orow)
-        const uint32_t tlane = tbase + ((uint32_t)(32 * q) << 16) + kColO + cg * kCols;
-        const size_t col0 = (size_t)r * kNv + cg * kCols;
-        const __nv_bfloat16 *zg = reinterpret_cast<const __nv_bfloat16 *>(p.z);
-        __nv_bfloat16 *outg = reinterpret_cast<__nv_bfloat16 *>(p.out);
-        const uint32_t my_rank = kNorm ? cluster_ctarank() : 0;
-        for (int c = 0; c < nck; ++c) {
-            const int pp = c & 1;
-            const int Lc = min(kC, len - c * kC);
-            const size_t oidx = ((size_t)(tok0 + c * kC + orow) * hv + h) * kD + col0;
-            float zc[kCols];
-            if (kNorm && orow < Lc) {   // z of this chunk, loaded while the MMAs run
-                unpack8(reinterpret_cast<const uint4 *>(zg + oidx)[0], *reinterpret_cast<float(*)[8]>(zc));
-                unpack8(reinterpret_cast<const uint4 *>(zg + oidx)[1], *reinterpret_cast<float(*)[8]>(zc + 8));
-            }
-            wait_bar(s, &s->bar_out[pp], (uint32_t)(c >> 1) & 1, p.status);
-            tc_fence_after();
-            float o[kCols];
-            tmem_ld16(tlane + pp * kNv, o);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&s->ofree[pp]);
-            float ss = 0.f;
-#pragma unroll
-            for (int j = 0; j < kCols; ++j) {
-                o[j] *= kScale;
-                ss = fmaf(o[j], o[j], ss);
-            }
-            if (kNorm) {
-                // row sums over this CTA's 32 columns, pushed to all four
-                // CTAs' receive buffers (slot = this CTA's rank)
-                s->red_local[pp][cg][orow] = ss;
-                named_sync(kBarRed, kCntRed);
-                if (cg == 0) {
-                    if (orow == 0)
-                        mbar_arrive_expect_tx(&s->red_full[pp], kTiles * 64 * 4);
-                    const float t = s->red_local[pp][0][orow] + s->red_local[pp][1][orow];
-#pragma unroll
-                    for (uint32_t rk = 0; rk < kTiles; ++rk)
-                        st_async_remote(&s->red_in[pp][my_rank][orow], t, &s->red_full[pp], rk);
-                }
-                const bool ok = wait_bar_cluster(s, &s->red_full[pp], (uint32_t)(c >> 1) & 1, p.status);
-                if (ok && orow < Lc) {
-                    float tot = 0.f;
-#pragma unroll
-                    for (int rk = 0; rk < kTiles; ++rk)
-                        tot += s->red_in[pp][rk][orow];
-                    const float rn = rsqrtf(tot * (1.f / kD) + p.eps);
-#pragma unroll
-                    for (int j = 0; j < kCols; ++j)
-                        o[j] = o[j] * rn * s->w[cg * kCols + j] * (zc[j] * sigmoid_f(zc[j]));
-                }
-            }
-            if (orow < Lc) {
-                float o8[8];
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) o8[j] = o[8 * hh + j];
-                    reinterpret_cast<uint4 *>(outg + oidx)[hh] = pack8(o8);
-                }
-            }
-        }
     }
 
-    if (kNorm) {   // peers may still be reading this CTA's partial sums
-        cluster_arrive();
-        cluster_wait();
-    }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -414,42 +298,18 @@ scan_kernel(PrefillArgs p)
 
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillArgs &p, cudaStream_t stream)
+cudaError_t launch_prefill_scan(const PrefillArgs &p, cudaStream_t stream)
 {
-    if (p.num_seqs == 0)
-        return cudaSuccess;
-    if (p.total_tokens > 0) {
-        cudaError_t e = launch_prefill_prep(p, stream);
-        if (e != cudaSuccess)
-            return e;
-    }
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(scan_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(scan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess)
             return e;
         configured = true;
     }
     dim3 grid(kTiles, p.hv, p.num_seqs);
-    if (!p.z) {
-        scan_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(p);
-        return cudaGetLastError();
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kTiles;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, scan_kernel<true>, p);
+    scan_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
+    return cudaGetLastError();
 }
 
 }  // namespace gdn

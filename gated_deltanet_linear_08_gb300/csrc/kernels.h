@@ -35,26 +35,26 @@ struct PrefillArgs {
 };
 
 // Workspace layout of the chunked prefill (all offsets 1024-byte aligned).
-// Per (chunk, value head) one 89 KB record of fp16 byte-exact shared-memory
-// operand images (see tc05.cuh), in the order the scan kernel stages them:
+// Per (chunk, value head) one 121 KB record of fp16 byte-exact shared-memory
+// operand images (see tc05.cuh), ordered so that the scan kernel copies its
+// operands (Mc, Ec) and the output kernel its operands (Qc, Fc, V, S) each as
+// one contiguous run:
 //   Mc  128x128  state-to-state map -Kn^T diag(eps) W, K-major 128B swizzle,
-//                two 64-wide K halves of 16 KB (at 0 and 24 KB)
-//   Qc   64x128  state-to-output map diag(Gam r_q) Q - R, K-major, two K
-//                halves of 8 KB (at 16 KB and 40 KB, each directly after a
-//                Mc half, so a 128-row operand starting 8 KB earlier has
-//                Qc as rows 64-127)
-//   Ec  128x64   value-to-state map Kn^T diag(eps) T diag(beta), K-major (48 KB)
-//   Fc   64x64   value-to-output map P T diag(beta), K-major (64 KB, after Ec)
-//   V   [token 64][dv 32] x 4 value slices, MN-major 64B swizzle (72 KB)
-//   scal fp32 e^{G_last} (88 KB)
+//                two 64-wide K halves of 16 KB                         [0, 32K)
+//   Ec  128x64   value-to-state map Kn^T diag(eps) T diag(beta)       [32K, 48K)
+//   Qc   64x128  state-to-output map diag(Gam r_q) Q - R, two K halves
+//                of 8 KB                                               [48K, 64K)
+//   Fc   64x64   value-to-output map P T diag(beta)                    [64K, 72K)
+//   V   [token 64][dv 32] x 4 value slices, MN-major 64B swizzle       [72K, 88K)
+//   S   [dk 128][dv 32] x 4 value slices: the fp16 state entering the
+//       chunk, written by the scan kernel, MN-major 64B swizzle        [88K, 120K)
+//   scal fp32 e^{G_last}                                               [120K]
 // with eps_i = e^{G_last - G_i} for the chunk's valid rows, 0 past them.
-constexpr size_t kWsMc0 = 0, kWsQc0 = 16384, kWsMc1 = 24576, kWsQc1 = 40960;
-constexpr size_t kWsEc = 49152, kWsFc = 65536;
-constexpr size_t kOpsBytes = 73728;          // Mc, Qc, Ec, Fc
-constexpr size_t kWsV = 73728;
-constexpr size_t kVBytes = 16384;
-constexpr size_t kWsScal = 90112;
-constexpr size_t kPerVHead = 91136;
+constexpr size_t kWsMc0 = 0, kWsMc1 = 16384, kWsEc = 32768;
+constexpr size_t kWsQc0 = 49152, kWsQc1 = 57344, kWsFc = 65536;
+constexpr size_t kWsV = 73728, kWsS = 90112, kWsScal = 122880;
+constexpr size_t kVBytes = 16384, kSBytes = 32768;
+constexpr size_t kPerVHead = 123904;
 
 inline int prefill_max_chunks(int num_seqs, int total_tokens)
 {
@@ -70,6 +70,25 @@ inline size_t prefill_workspace_bytes(int num_seqs, int total_tokens, int hk, in
 }
 
 cudaError_t launch_decode(const DecodeArgs &args, cudaStream_t stream);
-cudaError_t launch_prefill(const PrefillArgs &args, cudaStream_t stream);
+// The chunked prefill runs three kernels in stream order: prep (chunk-parallel
+// maps), scan (serial state chain, one CTA per sequence, head and Dv slice)
+// and out (chunk-parallel outputs and epilogue).
+cudaError_t launch_prefill_prep(const PrefillArgs &args, cudaStream_t stream);
+cudaError_t launch_prefill_scan(const PrefillArgs &args, cudaStream_t stream);
+cudaError_t launch_prefill_out(const PrefillArgs &args, cudaStream_t stream);
+inline cudaError_t launch_prefill(const PrefillArgs &args, cudaStream_t stream)
+{
+    if (args.num_seqs == 0)
+        return cudaSuccess;
+    if (args.total_tokens > 0) {
+        cudaError_t e = launch_prefill_prep(args, stream);
+        if (e != cudaSuccess)
+            return e;
+    }
+    cudaError_t e = launch_prefill_scan(args, stream);
+    if (e != cudaSuccess || args.total_tokens == 0)
+        return e;
+    return launch_prefill_out(args, stream);
+}
 
 }  // namespace gdn
