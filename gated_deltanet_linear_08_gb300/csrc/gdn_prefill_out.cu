@@ -3,15 +3,25 @@
 // inference kernels", Summary: chunked kernel followed by a fused gated
 // RMSNorm o * rsqrt(mean(o^2) + eps) * w * silu(z)).
 //
-// One CTA per (64-token chunk, value head), all chunks at once: with S the
-// fp16 state entering the chunk (written by the scan kernel) and the chunk's
-// maps from the prep kernel,
+// All (chunk, value head) units are independent: with S the fp16 state
+// entering the chunk (written by the scan kernel) and the chunk's maps from
+// the prep kernel,
 //   o = scale [Qc | Fc] [S; V]          tcgen05, M = 128, N = 128, K = 192
 // The record stores Qc's two K halves and Fc back to back, so a 128-row
 // operand starting at any of them has it as rows 0-63 (rows 64-127 are the
 // next image and are ignored): the outputs land in TMEM lanes 0-63, one token
 // row per lane, and the norm over Dv needs only the two threads that share a
 // row.
+//
+// A persistent grid (one CTA per SM) walks the units with a two-stage
+// pipeline, so the copies for the next unit overlap this unit's products and
+// epilogue:
+//   warp 2      loads a unit's [Qc | Fc | V | S] run and its z tile
+//   warp 3      issues the 12 MMAs into one of two TMEM accumulators
+//   warps 0, 1, 4, 5, 8, 9, 12, 13
+//               epilogue (TMEM lanes 0-63 are readable by warps w with
+//               w % 4 < 2): scale, gated RMSNorm, bf16 tile, tensor-map store
+//   the other warps idle
 #include "common.cuh"
 #include "kernels.h"
 #include "tc05.cuh"
@@ -19,17 +29,26 @@
 namespace gdn {
 namespace {
 
-constexpr int kThreads = 256;
-// Shared memory: the record's [Qc | Fc | V | S] run (72 KB) as copied.
+constexpr int kThreads = 16 * 32;
+constexpr int kLoaderWarp = 2, kIssuerWarp = 3;
+// Stage: the record's [Qc | Fc | V | S] run (72 KB) as copied, then the unit's
+// 64 x 128 bf16 tile of z (tensor-map copy, dk halves of 8 KB, 128-byte
+// swizzle), which the epilogue overwrites with the outputs.
 constexpr uint32_t kOffQc0 = 0, kOffQc1 = 8192, kOffFc = 16384, kOffV = 24576, kOffS = 40960;
 constexpr uint32_t kRunBytes = 73728;
-constexpr uint32_t kOffSmall = kRunBytes;
-constexpr uint32_t kTmemCols = 128;
+constexpr uint32_t kOffY = kRunBytes;
+constexpr uint32_t kStageBytes = kRunBytes + 16384;
+constexpr int kStages = 2;
+constexpr uint32_t kOffSmall = kStages * kStageBytes;
+constexpr uint32_t kTmemCols = 256;          // two 128-column accumulators
+constexpr uint32_t kBarEpi = 1, kCntEpi = 256;   // the eight epilogue warps
 constexpr float kScale = 0.088388347648318440550f;  // 1/sqrt(128)
 
 struct Small {
-    float red[2][64];   // row sums of squares of each 64-column half
-    uint64_t mbar_ld, mbar_mma;
+    float red[4][64];          // row sums of squares of each 32-column quarter
+    uint64_t full[kStages];    // run and z tile landed
+    uint64_t mfull[kStages];   // accumulator written
+    uint64_t efree[kStages];   // epilogue done: tile stored, accumulator read
     uint32_t tmem_base;
     int fail;
 };
@@ -53,129 +72,206 @@ __device__ bool locate_chunk(const PrefillArgs &p, int gc, int &tok0, int &L)
     return false;
 }
 
-__device__ __forceinline__ void wait_bar(Small *s, uint64_t *bar, uint32_t parity, uint32_t *status)
+__device__ __forceinline__ bool wait_bar(Small *s, uint64_t *bar, uint32_t parity, uint32_t *status)
 {
     if (*reinterpret_cast<volatile int *>(&s->fail))
-        return;
+        return false;
     if (!mbar_wait(bar, parity)) {
         s->fail = 1;
         set_status(status, kStatusWaitTimeout);
+        return false;
     }
+    return true;
 }
 
 template <bool kNorm>
-__global__ void __launch_bounds__(kThreads, 2)
-out_kernel(PrefillArgs p)
+__global__ void __launch_bounds__(kThreads, 1)
+out_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_o)
 {
-    const int gc = blockIdx.x, h = blockIdx.y, hv = p.hv;
+    const int hv = p.hv, units = p.max_chunks * hv;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    int tok0 = 0, L = 0;
-    if (!locate_chunk(p, gc, tok0, L))
-        return;
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Small *s = reinterpret_cast<Small *>(sm + kOffSmall);
     const uint32_t sbase = smem_u32(sm);
-    const unsigned char *rec = p.workspace + ((size_t)gc * hv + h) * kPerVHead;
 
     if (tid == 0) {
-        mbar_init(&s->mbar_ld, 1);
-        mbar_init(&s->mbar_mma, 1);
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&s->full[i], 1);
+            mbar_init(&s->mfull[i], 1);
+            mbar_init(&s->efree[i], 1);
+        }
         mbar_fence_init();
         s->fail = 0;
-        mbar_arrive_expect_tx(&s->mbar_ld, kRunBytes);
-#pragma unroll
-        for (int k = 0; k < 3; ++k)
-            bulk_g2s(sm + k * 24576, rec + kWsQc0 + k * 24576, 24576, &s->mbar_ld);
     }
     if (warp == 0) {
         tmem_alloc(&s->tmem_base, kTmemCols);
         tmem_relinquish();
         tc_fence_before();
     }
-    // warps 0-1 and 4-5: token row 32 (w % 4) + lane, value columns 64 (w / 4) ..
-    const int q = warp & 3, ch = warp >> 2;
-    const int row = 32 * q + lane;
-    const bool outw = q < 2;
-    const size_t oidx = ((size_t)(tok0 + row) * hv + h) * kD + ch * 64;
-    uint4 zr[8];
-    if (kNorm && outw && row < L) {   // z of this row, loaded under the copy and the MMA
-        const uint4 *zs = reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(p.z) + oidx);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) zr[j] = zs[j];
-    }
     __syncthreads();
-    if (warp == 0) {
-        tc_fence_after();
+    tc_fence_after();
+    const uint32_t tbase = s->tmem_base;
+    // Every role walks the same units (u = chunk * Hv + head, strided by the
+    // grid) and counts only the live ones, so stage k % 2 and barrier phases
+    // agree across roles.
+
+    if (warp == kLoaderWarp) {
+        // ------------------------------------------------------------ loader
         if (lane == 0) {
-            wait_bar(s, &s->mbar_ld, 0, p.status);
-            if (!*reinterpret_cast<volatile int *>(&s->fail)) {
-                constexpr uint32_t idesc = make_idesc_f16(128, 128, false, true);
-                const uint64_t bv = make_desc(sbase + kOffV, 4096, 512, kSw64);
-                const uint64_t bs = make_desc(sbase + kOffS, 8192, 512, kSw64);
-                const uint64_t af = make_desc(sbase + kOffFc, 16, 1024, kSw128);
+            int k = 0, issued[kStages] = {0, 0};
+            for (int u = blockIdx.x; u < units; u += gridDim.x) {
+                const int gc = u / hv, h = u - gc * hv;
+                int tok0 = 0, L = 0;
+                if (!locate_chunk(p, gc, tok0, L))
+                    continue;
+                const int st = k & 1;
+                // the unit two before used this stage: its tile must be stored
+                if (k >= kStages && !wait_bar(s, &s->efree[st], ((uint32_t)(k >> 1) & 1) ^ 1, p.status))
+                    break;
+                unsigned char *stage = sm + st * kStageBytes;
+                const unsigned char *rec = p.workspace + ((size_t)gc * hv + h) * kPerVHead;
+                mbar_arrive_expect_tx(&s->full[st], kRunBytes + (kNorm ? 16384u : 0u));
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)   // Fc V over the chunk's 64 tokens
-                    mma_f16(s->tmem_base, af + (uint64_t)(kk * 2), bv + (uint64_t)(kk * 64), idesc, kk != 0);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {  // Qc S over the 128 state rows
-                    const uint64_t aq = make_desc(sbase + (kk < 4 ? kOffQc0 : kOffQc1), 16, 1024, kSw128);
-                    mma_f16(s->tmem_base, aq + (uint64_t)((kk & 3) * 2), bs + (uint64_t)(kk * 64), idesc, 1u);
+                for (int j = 0; j < 3; ++j)
+                    bulk_g2s(stage + j * 24576, rec + kWsQc0 + j * 24576, 24576, &s->full[st]);
+                if (kNorm) {
+                    tma_load_3d(stage + kOffY, &tm_z, 0, h, tok0, &s->full[st]);
+                    tma_load_3d(stage + kOffY + 8192, &tm_z, 64, h, tok0, &s->full[st]);
                 }
+                ++issued[st];
+                ++k;
             }
-            mma_commit(&s->mbar_mma);
+            // no copy may still be landing in shared memory when the CTA exits
+            if (*reinterpret_cast<volatile int *>(&s->fail)) {
+                for (int i = 0; i < kStages; ++i)
+                    if (issued[i] > 0)
+                        mbar_wait(&s->full[i], (uint32_t)(issued[i] - 1) & 1);
+            }
         }
         __syncwarp();
-    }
-    if (outw) {
-        wait_bar(s, &s->mbar_mma, 0, p.status);
-        tc_fence_after();
-        float o[64];
-        {
-            float d[32];
-            tmem_ld32(s->tmem_base + ((uint32_t)(32 * q) << 16) + ch * 64, d);
+    } else if (warp == kIssuerWarp) {
+        // ------------------------------------------------------------ issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = make_idesc_f16(128, 128, false, true);
+            int k = 0;
+            for (int u = blockIdx.x; u < units; u += gridDim.x) {
+                int tok0 = 0, L = 0;
+                if (!locate_chunk(p, u / hv, tok0, L))
+                    continue;
+                const int st = k & 1;
+                const uint32_t stg = sbase + st * kStageBytes, d = tbase + st * 128;
+                bool ok = wait_bar(s, &s->full[st], (uint32_t)(k >> 1) & 1, p.status);
+                if (ok && k >= kStages)   // accumulator st read by the epilogue two units ago
+                    ok = wait_bar(s, &s->efree[st], ((uint32_t)(k >> 1) & 1) ^ 1, p.status);
+                if (ok) {
+                    tc_fence_after();
+                    const uint64_t bv = make_desc(stg + kOffV, 4096, 512, kSw64);
+                    const uint64_t bs = make_desc(stg + kOffS, 8192, 512, kSw64);
+                    const uint64_t af = make_desc(stg + kOffFc, 16, 1024, kSw128);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = d[j] * kScale;
-            tmem_ld32(s->tmem_base + ((uint32_t)(32 * q) << 16) + ch * 64 + 32, d);
+                    for (int kk = 0; kk < 4; ++kk)   // Fc V over the chunk's 64 tokens
+                        mma_f16(d, af + (uint64_t)(kk * 2), bv + (uint64_t)(kk * 64), idesc, kk != 0);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) o[32 + j] = d[j] * kScale;
-        }
-        if (kNorm) {
-            float ss = 0.f;
-#pragma unroll
-            for (int j = 0; j < 64; ++j) ss = fmaf(o[j], o[j], ss);
-            s->red[ch][row] = ss;
-            named_sync(1, 128);   // the four output warps
-            const float rn = rsqrtf((s->red[0][row] + s->red[1][row]) * (1.f / kD) + p.eps);
-            const __nv_bfloat16 *wg = reinterpret_cast<const __nv_bfloat16 *>(p.norm_w) + ch * 64;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                float zf[8], wf[8];
-                unpack8(zr[j], zf);
-                unpack8(reinterpret_cast<const uint4 *>(wg)[j], wf);
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    o[8 * j + e] = o[8 * j + e] * rn * wf[e] * (zf[e] * sigmoid_f(zf[e]));
+                    for (int kk = 0; kk < 8; ++kk) {  // Qc S over the 128 state rows
+                        const uint64_t aq = make_desc(stg + (kk < 4 ? kOffQc0 : kOffQc1), 16, 1024, kSw128);
+                        mma_f16(d, aq + (uint64_t)((kk & 3) * 2), bs + (uint64_t)(kk * 64), idesc, 1u);
+                    }
+                }
+                mma_commit(&s->mfull[st]);
+                ++k;
             }
         }
-        if (row < L) {
-            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + oidx);
+        __syncwarp();
+    } else if ((warp & 3) < 2) {
+        // ------------------------------------------------------------ epilogue
+        // token row 32 (w % 4) + lane, value columns 32 (w / 4) .. + 31
+        const int q = warp & 3, cq = warp >> 2;
+        const int row = 32 * q + lane;
+        int k = 0;
+        for (int u = blockIdx.x; u < units; u += gridDim.x) {
+            const int gc = u / hv, h = u - gc * hv;
+            int tok0 = 0, L = 0;
+            if (!locate_chunk(p, gc, tok0, L))
+                continue;
+            const int st = k & 1;
+            // this thread's 32 columns: 16-byte chunks 4 (cq & 1) .. of dk half cq / 2
+            unsigned char *yt = sm + st * kStageBytes + kOffY + (cq >> 1) * 8192;
+            const int c0 = (cq & 1) * 4;
+            wait_bar(s, &s->full[st], (uint32_t)(k >> 1) & 1, p.status);      // z tile visible
+            wait_bar(s, &s->mfull[st], (uint32_t)(k >> 1) & 1, p.status);
+            tc_fence_after();
+            float o[32];
+            tmem_ld32(tbase + st * 128 + ((uint32_t)(32 * q) << 16) + cq * 32, o);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                float v[8];
+            for (int j = 0; j < 32; ++j) o[j] *= kScale;
+            if (kNorm) {
+                float ss = 0.f;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = o[8 * j + e];
-                dst[j] = pack8(v);
+                for (int j = 0; j < 32; ++j) ss = fmaf(o[j], o[j], ss);
+                s->red[cq][row] = ss;
+                named_sync(kBarEpi, kCntEpi);
+                const float rn = rsqrtf((s->red[0][row] + s->red[1][row] + s->red[2][row] + s->red[3][row])
+                                        * (1.f / kD) + p.eps);
+                const __nv_bfloat16 *wg = reinterpret_cast<const __nv_bfloat16 *>(p.norm_w) + cq * 32;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float zf[8], wf[8];
+                    unpack8(*reinterpret_cast<const uint4 *>(yt + sw128_chunk_offset(row, c0 + j)), zf);
+                    unpack8(reinterpret_cast<const uint4 *>(wg)[j], wf);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)   // silu(z) = z / (1 + e^-z)
+                        o[8 * j + e] = o[8 * j + e] * rn * wf[e] * __fdividef(zf[e], 1.f + __expf(-zf[e]));
+                }
             }
+            if (L == kC) {
+                // whole chunk: bf16 outputs into the tile, one tensor-map store per dk half
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = o[8 * j + e];
+                    *reinterpret_cast<uint4 *>(yt + sw128_chunk_offset(row, c0 + j)) = pack8(v);
+                }
+                fence_async_smem();
+            } else if (row < L) {
+                // a sequence's ragged last chunk: the rows past it belong to the
+                // next sequence, so each valid row is stored on its own
+                uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out)
+                                                       + ((size_t)(tok0 + row) * hv + h) * kD + cq * 32);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = o[8 * j + e];
+                    dst[j] = pack8(v);
+                }
+            }
+            tc_fence_before();
+            named_sync(kBarEpi, kCntEpi);   // accumulator read, tile complete, red consumed
+            if (tid == 0) {
+                if (L == kC) {
+                    unsigned char *tile = sm + st * kStageBytes + kOffY;
+                    tma_store_3d(&tm_o, 0, h, tok0, tile);
+                    tma_store_3d(&tm_o, 64, h, tok0, tile + 8192);
+                    bulk_commit();
+                    bulk_wait_read<0>();
+                }
+                mbar_arrive(&s->efree[st]);
+            }
+            ++k;
         }
+        if (tid == 0)
+            bulk_wait_all();
     }
+
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(s->tmem_base, kTmemCols);
+        tmem_dealloc(tbase, kTmemCols);
     }
 }
 
@@ -192,11 +288,30 @@ cudaError_t launch_prefill_out(const PrefillArgs &p, cudaStream_t stream)
             return e;
         configured = true;
     }
-    dim3 grid(p.max_chunks, p.hv);
+    CUtensorMap tz, to;
+    if (!encode_tile_map(&to, p.out, p.hv, p.total_tokens))
+        return cudaErrorInvalidValue;
+    if (p.z) {
+        if (!encode_tile_map(&tz, p.z, p.hv, p.total_tokens))
+            return cudaErrorInvalidValue;
+    } else {
+        tz = to;   // unused without the epilogue
+    }
+    static int sm_count[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return cudaErrorInvalidDevice;
+    if (!sm_count[dev]) {
+        cudaError_t e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return e;
+    }
+    const int units = p.max_chunks * p.hv;
+    const dim3 grid(units < sm_count[dev] ? units : sm_count[dev]);
     if (p.z)
-        out_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(p);
+        out_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(p, tz, to);
     else
-        out_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(p);
+        out_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(p, tz, to);
     return cudaGetLastError();
 }
 

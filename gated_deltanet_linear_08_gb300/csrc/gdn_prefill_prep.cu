@@ -72,6 +72,12 @@ constexpr uint32_t kOffAd = kOffXs + 3 * 512;
 constexpr uint32_t kOffBE = 73728;
 constexpr uint32_t kOffBM = kOffBE + 8192;
 constexpr uint32_t kOffSmall = kOffBM + 16384;
+// Staging of the images bulk-copied to the workspace (regions free at the time).
+constexpr uint32_t kOffStV = kOffBE;     // V slices, until BE is written
+constexpr uint32_t kOffStFc = kOffTb;    // Fc, after MT
+constexpr uint32_t kOffStEc = kOffAh;    // Ec (16 KB up to BE), after the inverse
+constexpr uint32_t kOffStQc = kOffP;     // Qc, after [W; R]
+constexpr uint32_t kOffStMc = kOffKQ;    // Mc, after Mc
 constexpr uint32_t kTmaBytes = 6 * 8192;   // k, q, v: two 64x64 bf16 boxes each
 
 // TMEM: D_a in [0,64), MT in [64,128); then Ec in [0,64) and [W; R] in
@@ -291,7 +297,8 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
             float f[8];
-            unpack8(*reinterpret_cast<const uint4 *>(sm + rb + c * 16), f);
+            // rotate the chunk by row so the lanes of a warp hit distinct banks
+            unpack8(*reinterpret_cast<const uint4 *>(sm + rb + ((c + i) & 7) * 16), f);
 #pragma unroll
             for (int e = 0; e < 8; ++e)
                 ss = fmaf(f[e], f[e], ss);
@@ -321,7 +328,8 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
         __syncwarp();
     }
 
-    // ---- 3. v -> four fp16 [token][32] value-slice images in the workspace
+    // ---- 3. v -> four fp16 [token][32] value-slice images, staged for one bulk
+    //         copy to the workspace
     {
         bool over = false;
 #pragma unroll
@@ -334,7 +342,7 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
             for (int j = 0; j < 8; ++j)
                 over |= !(fabsf(f[j]) <= kHalfMax);
             // value columns 8*c16..+7 sit in slice c16/4, 16-byte chunk c16%4
-            *reinterpret_cast<uint4 *>(ws + kWsV + (c16 >> 2) * 4096 + sw64_chunk_offset(i, c16 & 3)) = pack8h(f);
+            *reinterpret_cast<uint4 *>(sm + kOffStV + (c16 >> 2) * 4096 + sw64_chunk_offset(i, c16 & 3)) = pack8h(f);
         }
         if (over)
             set_status(p.status, kStatusRange);
@@ -355,7 +363,10 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
         for (int j = 0; j < 8; ++j) f[j] *= rk;
         *ptr = pack8h(f);
     }
+    fence_async_smem();
     __syncthreads();   // the v tile is consumed before [I; P] overwrites it
+    if (tid == 0)
+        bulk_s2g(ws + kWsV, sm + kOffStV, (uint32_t)kVBytes);
 
     // ---- 4. A (fp16 blocks below the diagonal, fp32 diagonal blocks) from
     //         lanes 0-63 and P (fp16, rows 64-127 of [I; P]) from lanes
@@ -455,6 +466,8 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
     __syncthreads();
     if (warp == 0)
         merge_block(sm, s, 3, 0, lane, warp);
+    if (tid == 0)
+        bulk_wait_read<0>();   // the V copy has left the staging that BE reuses
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -495,7 +508,7 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
             const uint32_t off = sw128_chunk_offset(i, ch * 4 + c);
             *reinterpret_cast<uint4 *>(sm + kOffP + sw128_chunk_offset(row, ch * 4 + c)) = pack8h(a8);
             if (q >= 2) {
-                *reinterpret_cast<uint4 *>(ws + kWsFc + off) = pack8h(m8);
+                *reinterpret_cast<uint4 *>(sm + kOffStFc + off) = pack8h(m8);
             } else {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) m8[e] *= ei;
@@ -507,6 +520,8 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
     tc_fence_before();
     __syncthreads();
 
+    if (tid == 0)
+        bulk_s2g(ws + kWsFc, sm + kOffStFc, 8192);
     // ---- 8. Ec = Kn^T BE (TMEM [0,64); A = Kn read MN-major: dk halves 16 KB
     //         apart, 16-token steps of 2 KB) and [W; R] = A' Kn (TMEM
     //         [128,256); B = Kn read MN-major)
@@ -551,7 +566,7 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         w8[e] = fmaf(qs, qv[e], -dv[u * 8 + e]);
-                    *reinterpret_cast<uint4 *>(ws + (ch ? kWsQc1 : kWsQc0) + sw128_chunk_offset(i, c)) = pack8h(w8);
+                    *reinterpret_cast<uint4 *>(sm + kOffStQc + ch * 8192 + sw128_chunk_offset(i, c)) = pack8h(w8);
                 } else {
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
@@ -567,13 +582,17 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
             float e8[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) e8[e] = ev[c * 8 + e];
-            *reinterpret_cast<uint4 *>(ws + kWsEc + sw128_chunk_offset(row, ch * 4 + c)) = pack8h(e8);
+            *reinterpret_cast<uint4 *>(sm + kOffStEc + sw128_chunk_offset(row, ch * 4 + c)) = pack8h(e8);
         }
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
 
+    if (tid == 0) {
+        bulk_s2g(ws + kWsQc0, sm + kOffStQc, 16384);
+        bulk_s2g(ws + kWsEc, sm + kOffStEc, 16384);
+    }
     // ---- 10. Mc = Kn^T BM into TMEM [0,128) (Ec has been read)
     if (warp == 0) {
         tc_fence_after();
@@ -599,19 +618,27 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
             float m8[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) m8[e] = mv[u * 8 + e];
-            *reinterpret_cast<uint4 *>(ws + (ch ? kWsMc1 : kWsMc0) + sw128_chunk_offset(row, g * 4 + u)) = pack8h(m8);
+            *reinterpret_cast<uint4 *>(sm + kOffStMc + ch * 16384 + sw128_chunk_offset(row, g * 4 + u)) = pack8h(m8);
         }
     }
 
-    // ---- teardown
+    // ---- teardown: Mc out, and every staged copy complete before the CTA exits
+    fence_async_smem();
     tc_fence_before();
     __syncthreads();
+    if (tid == 0) {
+        bulk_s2g(ws + kWsMc0, sm + kOffStMc, 32768);
+        bulk_wait_all();
+    }
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(s->tmem_base, kTmemCols);
     }
 }
 
+}  // namespace
+
+namespace {
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -630,6 +657,8 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
+}  // namespace
+
 // Tensor map over a bf16 [T][heads][128] tensor: boxes of 64 tokens x 64
 // dims of one head, 128-byte swizzled in shared memory, zero fill past T.
 bool encode_tile_map(CUtensorMap *map, const void *base, int heads, int tokens)
@@ -646,7 +675,6 @@ bool encode_tile_map(CUtensorMap *map, const void *base, int heads, int tokens)
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
 
 cudaError_t launch_prefill_prep(const PrefillArgs &p, cudaStream_t stream)
 {

@@ -118,20 +118,6 @@ __device__ __forceinline__ void issue_mcs(uint32_t d, uint32_t st, uint64_t ds, 
         mma_f16(d, (kk < 4 ? a0 : a1) + (uint64_t)((kk & 3) * 2), ds + (uint64_t)(kk * 64), idesc, 1u);
 }
 
-// Bulk shared -> global copy in the issuing thread's bulk group.
-__device__ __forceinline__ void bulk_s2g(void *dst_gmem, const void *src_smem, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-                 :: "l"(dst_gmem), "r"(smem_u32(src_smem)), "r"(bytes) : "memory");
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// Wait until at most N of this thread's bulk groups still read shared memory.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read()
-{
-    asm volatile("cp.async.bulk.wait_group.read %0;" :: "n"(N) : "memory");
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
 scan_kernel(PrefillArgs p)
 {
@@ -183,15 +169,15 @@ scan_kernel(PrefillArgs p)
             __syncwarp();
             named_sync(kBarS, kCntS);            // S(c) operand written
             if (lane == 0) {
+                if (!failed(s)) {
+                    tc_fence_after();
+                    issue_mcs(dS, sst, make_desc(sbase + kOffS + b * 8192, 512, 512, kSw64), idesc);
+                }
                 // the S(c) operand -> workspace, for the output kernel; the copy
                 // of S(c-1) must have finished reading its buffer before the
                 // state warps (released by this chunk's chain) overwrite it
                 bulk_s2g(record(c) + kWsS + r * 8192, sm + kOffS + b * 8192, 8192);
                 bulk_wait_read<1>();
-                if (!failed(s)) {
-                    tc_fence_after();
-                    issue_mcs(dS, sst, make_desc(sbase + kOffS + b * 8192, 512, 512, kSw64), idesc);
-                }
                 mma_commit(&s->bar_chain);
                 mma_commit(&s->sfree[st]);
                 pre = false;
@@ -205,7 +191,7 @@ scan_kernel(PrefillArgs p)
             __syncwarp();
         }
         if (lane == 0)
-            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");   // every S copy complete before exit
+            bulk_wait_all();   // every S copy complete before exit
         __syncwarp();
     } else if (warp == kLoaderWarp) {
         // ------------------------------------------------------------ loader
@@ -268,9 +254,11 @@ scan_kernel(PrefillArgs p)
         };
         if (nck > 0)
             put_state(0);
+        // e^{G_last} of chunks c and c+1 in registers, c+2 requested two chunks ahead
         float gl = (nck > 0) ? *reinterpret_cast<const float *>(record(0) + kWsScal) : 0.f;
+        float gl1 = (nck > 1) ? *reinterpret_cast<const float *>(record(1) + kWsScal) : 0.f;
         for (int c = 0; c < nck; ++c) {
-            const float gnext = (c + 1 < nck) ? *reinterpret_cast<const float *>(record(c + 1) + kWsScal) : 0.f;
+            const float gl2 = (c + 2 < nck) ? *reinterpret_cast<const float *>(record(c + 2) + kWsScal) : 0.f;
             wait_bar(s, &s->bar_chain, (uint32_t)c & 1, p.status);
             tc_fence_after();
             float dv[kCols];
@@ -279,7 +267,8 @@ scan_kernel(PrefillArgs p)
             for (int j = 0; j < kCols; ++j) S[j] = fmaf(gl, S[j], dv[j]);
             if (c + 1 < nck)
                 put_state((c + 1) & 1);
-            gl = gnext;
+            gl = gl1;
+            gl1 = gl2;
         }
         if (over)
             set_status(p.status, kStatusRange);

@@ -4,6 +4,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace gdn {
@@ -68,6 +69,12 @@ inline size_t prefill_workspace_bytes(int num_seqs, int total_tokens, int hk, in
     const size_t c = (size_t)prefill_max_chunks(num_seqs, total_tokens);
     return c * (size_t)hv * kPerVHead;
 }
+
+// Tensor map over a bf16 [tokens][heads][128] tensor: boxes of 64 tokens x 64
+// dims of one head, 128-byte swizzled in shared memory, zero fill past the
+// last token.  Host only; false if the driver's encoder is unavailable or
+// rejects the tensor.
+bool encode_tile_map(CUtensorMap *map, const void *base, int heads, int tokens);
 
 cudaError_t launch_decode(const DecodeArgs &args, cudaStream_t stream);
 // The chunked prefill runs three kernels in stream order: prep (chunk-parallel

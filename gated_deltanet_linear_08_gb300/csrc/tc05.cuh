@@ -320,6 +320,23 @@ __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, u
                  : "memory");
 }
 
+// Bulk shared -> global copy, committed as its own bulk group of the issuing
+// thread (both addresses 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_s2g(void *dst_gmem, const void *src_smem, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 :: "l"(dst_gmem), "r"(smem_u32(src_smem)), "r"(bytes) : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" :: "n"(N) : "memory");
+}
+// Wait until every bulk group of this thread has completed (writes visible).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Tiled 3-D tensor copy global -> shared through a tensor map (a CUtensorMap
 // kernel parameter), completing bytes on `mbar`.  c0 is the innermost
 // coordinate; c0 * element size must be a multiple of 16 bytes.  Boxes that
@@ -332,6 +349,16 @@ __device__ __forceinline__ void tma_load_3d(void *dst_smem, const void *tmap, in
                  :: "r"(smem_u32(dst_smem)), "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(mbar))
                  : "memory");
 }
+
+// Tiled 3-D tensor copy shared -> global through a tensor map, committed as a
+// bulk group of the issuing thread.  Only the part of the box inside the
+// tensor is written.
+__device__ __forceinline__ void tma_store_3d(const void *tmap, int c0, int c1, int c2, const void *src_smem)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];"
+                 :: "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src_smem)) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------
 // Warp-level 16x16 fp16 products for block algebra that is too small for a
