@@ -18,8 +18,8 @@
 
 namespace {
 
-// 64 MiB: each (64-token chunk, value head) takes 121 KB of scratch, so at
-// Hv = 32 this covers 16 chunks, about 1,000 packed tokens.  The extra 1 KB
+// 64 MiB: each (64-token chunk, value head) takes 137 KB of scratch, so at
+// Hv = 32 this covers 14 chunks, about 850 packed tokens.  The extra 1 KB
 // lets the base be rounded up to the 1024-byte alignment gdn_prefill requires.
 constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes + 1024];

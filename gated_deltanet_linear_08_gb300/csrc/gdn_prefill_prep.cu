@@ -19,10 +19,11 @@
 //   [W; R] = MT diag(Gam) Kn                tcgen05
 //   Ec   = Kn^T diag(eps) T diag(beta)      tcgen05 (A = Kn read MN-major)
 //   Mc   = -Kn^T diag(eps) W                tcgen05
+//   Bc   = Ec V                             tcgen05
 // Within the chunk the delta rule gives U = T diag(beta) V - W S0 (the
 // UT/WY form), S1 = e^{G_last} S0 + Kn^T diag(eps) U and outputs
 // scale (diag(Gam) Qn S0 + P U), so
-//   S1 = e^{G_last} S0 + Mc S0 + Ec V
+//   S1 = e^{G_last} S0 + Mc S0 + Bc,  Bc = Ec V
 //   o  = scale (Qc S0 + Fc V),  Qc = diag(Gam r_q) Q - R,  Fc = P T diag(beta)
 // and the serial scan needs one tensor-core product per chunk on its chain.
 // Everything is written as the fp16 swizzled byte images the scan and output
@@ -57,9 +58,10 @@ constexpr int kThreads = 256;
 //       blocks of A below the diagonal blocks (row-major), the ten lower
 //       blocks of T stored transposed, one scratch block per merging warp.
 //   Ad: fp32 diagonal 16x16 blocks of A.
+//   StV: fp16 V slices [token][32] x 4, kept to the end as the B operand of Bc.
 //   BE: fp16 diag(eps) T diag(beta) [token][64], MN-major B operand of Ec.
 //   BM: fp16 -diag(eps) W [token][dk], MN-major B operand of Mc, dk halves
-//       8 KB apart.
+//       8 KB apart (in place of BE, once Ec is computed).
 constexpr uint32_t kOffKQ = 0;
 constexpr uint32_t kOffQ = 8192;        // + h * 16384
 constexpr uint32_t kOffV = 32768;
@@ -69,19 +71,19 @@ constexpr uint32_t kOffAh = 57344;
 constexpr uint32_t kOffTh = kOffAh + 6 * 512;
 constexpr uint32_t kOffXs = kOffTh + 10 * 512;
 constexpr uint32_t kOffAd = kOffXs + 3 * 512;
-constexpr uint32_t kOffBE = 73728;
-constexpr uint32_t kOffBM = kOffBE + 8192;
+constexpr uint32_t kOffStV = 73728;      // fp16 V slices: bulk-copied out, and the B operand of Bc
+constexpr uint32_t kOffBE = 90112;
+constexpr uint32_t kOffBM = 90112;       // after Ec has been computed (BE no longer needed)
 constexpr uint32_t kOffSmall = kOffBM + 16384;
 // Staging of the images bulk-copied to the workspace (regions free at the time).
-constexpr uint32_t kOffStV = kOffBE;     // V slices, until BE is written
 constexpr uint32_t kOffStFc = kOffTb;    // Fc, after MT
-constexpr uint32_t kOffStEc = kOffAh;    // Ec (16 KB up to BE), after the inverse
+constexpr uint32_t kOffStEc = kOffAh;    // Ec as the fp16 A operand of Bc, after the inverse
 constexpr uint32_t kOffStQc = kOffP;     // Qc, after [W; R]
 constexpr uint32_t kOffStMc = kOffKQ;    // Mc, after Mc
 constexpr uint32_t kTmaBytes = 6 * 8192;   // k, q, v: two 64x64 bf16 boxes each
 
 // TMEM: D_a in [0,64), MT in [64,128); then Ec in [0,64) and [W; R] in
-// [128,256); then Mc in [0,128).
+// [128,256); then Mc in [0,128) and Bc in [128,256).
 constexpr uint32_t kTmemCols = 256;
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -466,8 +468,6 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
     __syncthreads();
     if (warp == 0)
         merge_block(sm, s, 3, 0, lane, warp);
-    if (tid == 0)
-        bulk_wait_read<0>();   // the V copy has left the staging that BE reuses
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -591,17 +591,23 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
 
     if (tid == 0) {
         bulk_s2g(ws + kWsQc0, sm + kOffStQc, 16384);
-        bulk_s2g(ws + kWsEc, sm + kOffStEc, 16384);
     }
-    // ---- 10. Mc = Kn^T BM into TMEM [0,128) (Ec has been read)
+    // ---- 10. Mc = Kn^T BM into TMEM [0,128) (Ec has been read) and
+    //          Bc = Ec V into [128,256) ([W; R] has been read); A = the fp16
+    //          Ec image, B = the V slices read MN-major (slices 4 KB apart)
     if (warp == 0) {
         tc_fence_after();
         if (lane == 0) {
             constexpr uint32_t idesc = make_idesc_f16(128, 128, true, true);
+            constexpr uint32_t idesc_b = make_idesc_f16(128, 128, false, true);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
                 mma_f16(s->tmem_base, make_desc(sbase + kOffKQ + kk * 2048, 16384, 1024, kSw128),
                         make_desc(sbase + kOffBM + kk * 2048, 8192, 1024, kSw128), idesc, kk != 0);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_f16(s->tmem_base + 128, make_desc(sbase + kOffStEc + kk * 32, 16, 1024, kSw128),
+                        make_desc(sbase + kOffStV + kk * 1024, 4096, 512, kSw64), idesc_b, kk != 0);
             mma_commit(&s->mbar_mma);
         }
         __syncwarp();
@@ -619,6 +625,23 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
 #pragma unroll
             for (int e = 0; e < 8; ++e) m8[e] = mv[u * 8 + e];
             *reinterpret_cast<uint4 *>(sm + kOffStMc + ch * 16384 + sw128_chunk_offset(row, g * 4 + u)) = pack8h(m8);
+        }
+    }
+
+    // Bc row = lane (dk), value columns 64 ch .. = slices 2 ch, 2 ch + 1, in
+    // 64-byte-swizzled rows: each thread writes one 64-byte row per slice, a
+    // warp 2 KB
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+        float bv[32];
+        tmem_ld32(s->tmem_base + ((uint32_t)(32 * q) << 16) + 128 + ch * 64 + g * 32, bv);
+        unsigned char *dst = ws + kWsBc + (2 * ch + g) * 8192;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            float b8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) b8[e] = bv[u * 8 + e];
+            *reinterpret_cast<uint4 *>(dst + sw64_chunk_offset(row, u)) = pack8h(b8);
         }
     }
 

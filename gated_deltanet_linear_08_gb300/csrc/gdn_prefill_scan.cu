@@ -8,19 +8,22 @@
 // is independent per value column, so the four slices of a head run in
 // parallel with no communication.
 //
-// The prep kernel turns each chunk into an affine map of the state (tcgen05,
-// M = 128, fp16 operands; S is the fp32 slice, 128 x 32):
-//   S' = e^{G_last} S + [Mc | Ec] [S; V]
-// Ec V does not depend on S and is issued ahead, so the serial chain per
-// chunk is S (fp16 operand) -> 8 MMAs -> TMEM -> S' in registers.  Each
-// chunk's fp16 S operand is also copied to the workspace, where the output
-// kernel, fully parallel over chunks, turns it into the chunk's outputs.
+// The prep kernel turns each chunk into an affine map of the state (S is the
+// fp32 slice, 128 x 32):
+//   S' = e^{G_last} S + Mc S + Bc
+// with Mc an fp16 tcgen05 operand (M = 128) and Bc, the value input, added
+// by the state threads.  The serial chain per chunk is S (fp16 operand) ->
+// 8 MMAs -> TMEM -> S' in registers; the state threads touch no global
+// memory inside it.  Each chunk's fp16 S operand is also copied to the
+// workspace, where the output kernel, fully parallel over chunks, turns it
+// into the chunk's outputs.
 //
 // Roles (10 warps):
 //   warps 0-7   state: warp w holds TMEM lane quadrant w % 4 = state rows
 //               32 (w % 4) .. +31 and value columns 16 (w / 4) .. +15
-//   warp 8      issues every MMA and the copies of S to the workspace
-//   warp 9      issues the operand copies (three stages of 52 KB)
+//   warp 8      issues every MMA and the copy of S to the workspace
+//   warp 9      issues the stage copies (four stages: Mc, this CTA's Bc
+//               slice, e^{G_last})
 #include "common.cuh"
 #include "kernels.h"
 #include "tc05.cuh"
@@ -40,13 +43,12 @@ constexpr int kNv = 32;                 // value columns per CTA
 constexpr int kTiles = kD / kNv;        // 4 CTAs per (sequence, head)
 constexpr int kCols = 16;               // value columns per thread
 
-// Stage: the chunk's Mc and Ec (one contiguous run of the record) and this
-// CTA's V slice.
-constexpr uint32_t kStEc = (uint32_t)kWsEc;
-constexpr uint32_t kStV = 49152;
-constexpr uint32_t kStageBytes = 53248;
-constexpr int kStages = 3;
-constexpr uint32_t kLoadBytes = 49152 + 4096;
+// Stage: the chunk's Mc (the first 32 KB of its record), this CTA's Bc slice
+// and e^{G_last}.
+constexpr uint32_t kStBc = 32768, kStScal = 40960;
+constexpr uint32_t kStageBytes = 41984;
+constexpr int kStages = 4;
+constexpr uint32_t kLoadBytes = 32768 + 8192 + 16;
 
 constexpr uint32_t kOffS = kStages * kStageBytes;   // two S operands [dk][32] fp16, MN-major, 8 KB each
 constexpr uint32_t kOffSmall = kOffS + 16384;
@@ -56,7 +58,7 @@ constexpr uint32_t kTmemCols = 64;
 
 struct Small {
     uint64_t full[kStages];     // stage landed (one arrival + bytes)
-    uint64_t sfree[kStages];    // every MMA reading the stage has completed
+    uint64_t sfree[kStages];    // stage read: the MMAs (one commit) and the eight state warps
     uint64_t bar_chain;
     uint32_t tmem_base;
     int fail;
@@ -75,6 +77,17 @@ __device__ __forceinline__ bool wait_bar(Small *s, uint64_t *bar, uint32_t parit
         return false;
     }
     return true;
+}
+
+// Wait that first tests without suspending: a phase that has already
+// completed costs one test.  Spins a little before suspending, for waits on
+// the state chain where the wake-up delay would add to every chunk.
+__device__ __forceinline__ bool wait_quick(Small *s, uint64_t *bar, uint32_t parity, uint32_t *status, int spins)
+{
+    for (int i = 0; i < spins; ++i)
+        if (mbar_test(bar, parity))
+            return true;
+    return wait_bar(s, bar, parity, status);
 }
 
 // Chunks that precede sequence n, with the same treatment of malformed
@@ -101,21 +114,13 @@ __device__ int chunk_base_of(const PrefillArgs &p, int n, int &tok0, int &len)
 // Descriptors of the stage operands (shared-memory byte address `st`).
 __device__ __forceinline__ uint64_t desc_k128(uint32_t addr) { return make_desc(addr, 16, 1024, kSw128); }
 
-// D = Ec V: four K steps over the chunk's 64 tokens.
-__device__ __forceinline__ void issue_ecv(uint32_t d, uint32_t st, uint32_t idesc)
-{
-    const uint64_t a = desc_k128(st + kStEc), b = make_desc(st + kStV, 512, 512, kSw64);
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-        mma_f16(d, a + (uint64_t)(kk * 2), b + (uint64_t)(kk * 64), idesc, kk != 0 ? 1u : 0u);
-}
-// D += Mc S over the two 64-wide K halves of the state.
+// D = Mc S over the two 64-wide K halves of the state.
 __device__ __forceinline__ void issue_mcs(uint32_t d, uint32_t st, uint64_t ds, uint32_t idesc)
 {
     const uint64_t a0 = desc_k128(st + (uint32_t)kWsMc0), a1 = desc_k128(st + (uint32_t)kWsMc1);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
-        mma_f16(d, (kk < 4 ? a0 : a1) + (uint64_t)((kk & 3) * 2), ds + (uint64_t)(kk * 64), idesc, 1u);
+        mma_f16(d, (kk < 4 ? a0 : a1) + (uint64_t)((kk & 3) * 2), ds + (uint64_t)(kk * 64), idesc, kk != 0);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -139,7 +144,7 @@ scan_kernel(PrefillArgs p)
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&s->full[i], 1);
-            mbar_init(&s->sfree[i], 1);
+            mbar_init(&s->sfree[i], kStateWarps + 1);
         }
         mbar_init(&s->bar_chain, 1);
         mbar_fence_init();
@@ -157,36 +162,28 @@ scan_kernel(PrefillArgs p)
 
     if (warp == kIssuerWarp) {
         // ------------------------------------------------------------ issuer
-        bool pre = false;   // Ec V of the current chunk already issued
         for (int c = 0; c < nck; ++c) {
             const int b = c & 1, st = c % kStages;   // S operand and accumulator buffer; stage
             const uint32_t sst = sbase + st * kStageBytes;
             const uint32_t dS = tbase + b * kNv;
-            if (lane == 0 && !pre && wait_bar(s, &s->full[st], (uint32_t)(c / kStages) & 1, p.status)) {
-                tc_fence_after();
-                issue_ecv(dS, sst, idesc);
+            bool ok = true;
+            if (lane == 0) {
+                // the copy of S(c-1) has read its buffer before this chunk's
+                // chain releases the state warps to write S(c+1) there
+                bulk_wait_read<0>();
+                ok = wait_quick(s, &s->full[st], (uint32_t)(c / kStages) & 1, p.status, 1);
             }
             __syncwarp();
             named_sync(kBarS, kCntS);            // S(c) operand written
             if (lane == 0) {
-                if (!failed(s)) {
+                if (ok && !failed(s)) {
                     tc_fence_after();
                     issue_mcs(dS, sst, make_desc(sbase + kOffS + b * 8192, 512, 512, kSw64), idesc);
                 }
-                // the S(c) operand -> workspace, for the output kernel; the copy
-                // of S(c-1) must have finished reading its buffer before the
-                // state warps (released by this chunk's chain) overwrite it
-                bulk_s2g(record(c) + kWsS + r * 8192, sm + kOffS + b * 8192, 8192);
-                bulk_wait_read<1>();
                 mma_commit(&s->bar_chain);
                 mma_commit(&s->sfree[st]);
-                pre = false;
-                const int ns = (c + 1) % kStages;
-                if (c + 1 < nck && !failed(s) && mbar_test(&s->full[ns], (uint32_t)((c + 1) / kStages) & 1)) {
-                    tc_fence_after();
-                    issue_ecv(tbase + (b ^ 1) * kNv, sbase + ns * kStageBytes, idesc);
-                    pre = true;
-                }
+                // S(c) -> workspace, for the output kernel
+                bulk_s2g(record(c) + kWsS + r * 8192, sm + kOffS + b * 8192, 8192);
             }
             __syncwarp();
         }
@@ -195,20 +192,21 @@ scan_kernel(PrefillArgs p)
         __syncwarp();
     } else if (warp == kLoaderWarp) {
         // ------------------------------------------------------------ loader
-        int issued[kStages] = {0, 0, 0};
+        int issued[kStages] = {0, 0, 0, 0};
         if (lane == 0) {
             for (int c = 0; c < nck; ++c) {
                 const int st = c % kStages;
-                // chunk c goes into the stage chunk c-3 used, once every MMA
-                // that read it has completed
+                // chunk c goes into the stage chunk c-4 used, once its MMAs and
+                // the state warps have read it
                 if (c >= kStages && !wait_bar(s, &s->sfree[st], (uint32_t)(c / kStages - 1) & 1, p.status))
                     break;
                 unsigned char *stage = sm + st * kStageBytes;
                 const unsigned char *rec = record(c);
                 mbar_arrive_expect_tx(&s->full[st], kLoadBytes);
-                bulk_g2s(stage, rec, 24576, &s->full[st]);
-                bulk_g2s(stage + 24576, rec + 24576, 24576, &s->full[st]);
-                bulk_g2s(stage + kStV, rec + kWsV + r * 4096, 4096, &s->full[st]);
+                bulk_g2s(stage, rec, 16384, &s->full[st]);
+                bulk_g2s(stage + 16384, rec + 16384, 16384, &s->full[st]);
+                bulk_g2s(stage + kStBc, rec + kWsBc + r * 8192, 8192, &s->full[st]);
+                bulk_g2s(stage + kStScal, rec + kWsScal, 16, &s->full[st]);
                 ++issued[st];
             }
             // no copy may still be landing in shared memory when the CTA exits
@@ -237,6 +235,7 @@ scan_kernel(PrefillArgs p)
             for (int j = 0; j < kCols; ++j) S[j] = 0.f;
         }
         bool over = false;   // a state value left the fp16 operand range
+        // S -> fp16 operand buffer b
         auto put_state = [&](int b) {
             float v[8];
 #pragma unroll
@@ -254,21 +253,30 @@ scan_kernel(PrefillArgs p)
         };
         if (nck > 0)
             put_state(0);
-        // e^{G_last} of chunks c and c+1 in registers, c+2 requested two chunks ahead
-        float gl = (nck > 0) ? *reinterpret_cast<const float *>(record(0) + kWsScal) : 0.f;
-        float gl1 = (nck > 1) ? *reinterpret_cast<const float *>(record(1) + kWsScal) : 0.f;
         for (int c = 0; c < nck; ++c) {
-            const float gl2 = (c + 2 < nck) ? *reinterpret_cast<const float *>(record(c + 2) + kWsScal) : 0.f;
-            wait_bar(s, &s->bar_chain, (uint32_t)c & 1, p.status);
+            const int st = c % kStages;
+            const unsigned char *stage = sm + st * kStageBytes;
+            wait_quick(s, &s->full[st], (uint32_t)(c / kStages) & 1, p.status, 1);   // Bc, e^{G_last} visible
+            wait_quick(s, &s->bar_chain, (uint32_t)c & 1, p.status, 256);
             tc_fence_after();
             float dv[kCols];
             tmem_ld16(tlane + (c & 1) * kNv, dv);
+            const float g = *reinterpret_cast<const float *>(stage + kStScal);
+            uint4 bc[2];
+            bc[0] = *reinterpret_cast<const uint4 *>(stage + kStBc + sw64_chunk_offset(row, 2 * cg));
+            bc[1] = *reinterpret_cast<const uint4 *>(stage + kStBc + sw64_chunk_offset(row, 2 * cg + 1));
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&s->sfree[st]);
+            const __half2 *hp = reinterpret_cast<const __half2 *>(bc);
 #pragma unroll
-            for (int j = 0; j < kCols; ++j) S[j] = fmaf(gl, S[j], dv[j]);
+            for (int j = 0; j < kCols / 2; ++j) {
+                const float2 f2 = __half22float2(hp[j]);
+                S[2 * j] = fmaf(g, S[2 * j], dv[2 * j] + f2.x);
+                S[2 * j + 1] = fmaf(g, S[2 * j + 1], dv[2 * j + 1] + f2.y);
+            }
             if (c + 1 < nck)
                 put_state((c + 1) & 1);
-            gl = gl1;
-            gl1 = gl2;
         }
         if (over)
             set_status(p.status, kStatusRange);

@@ -36,26 +36,28 @@ struct PrefillArgs {
 };
 
 // Workspace layout of the chunked prefill (all offsets 1024-byte aligned).
-// Per (chunk, value head) one 121 KB record of fp16 byte-exact shared-memory
-// operand images (see tc05.cuh), ordered so that the scan kernel copies its
-// operands (Mc, Ec) and the output kernel its operands (Qc, Fc, V, S) each as
-// one contiguous run:
+// Per (chunk, value head) one 137 KB record, ordered so that the scan kernel
+// copies its operand (Mc) and the output kernel its operands (Qc, Fc, V, S)
+// each as one contiguous run.  Images are fp16 byte-exact shared-memory
+// operand layouts (see tc05.cuh):
 //   Mc  128x128  state-to-state map -Kn^T diag(eps) W, K-major 128B swizzle,
 //                two 64-wide K halves of 16 KB                         [0, 32K)
-//   Ec  128x64   value-to-state map Kn^T diag(eps) T diag(beta)       [32K, 48K)
+//   Bc  [slice 4][dk 128][dv 32] fp16 in 64-byte-swizzled rows: the
+//       chunk's value input to the state, Kn^T diag(eps) T diag(beta) V,
+//       added by the scan's state threads                              [32K, 64K)
 //   Qc   64x128  state-to-output map diag(Gam r_q) Q - R, two K halves
-//                of 8 KB                                               [48K, 64K)
-//   Fc   64x64   value-to-output map P T diag(beta)                    [64K, 72K)
-//   V   [token 64][dv 32] x 4 value slices, MN-major 64B swizzle       [72K, 88K)
+//                of 8 KB                                               [64K, 80K)
+//   Fc   64x64   value-to-output map P T diag(beta)                    [80K, 88K)
+//   V   [token 64][dv 32] x 4 value slices, MN-major 64B swizzle       [88K, 104K)
 //   S   [dk 128][dv 32] x 4 value slices: the fp16 state entering the
-//       chunk, written by the scan kernel, MN-major 64B swizzle        [88K, 120K)
-//   scal fp32 e^{G_last}                                               [120K]
+//       chunk, written by the scan kernel, MN-major 64B swizzle        [104K, 136K)
+//   scal fp32 e^{G_last}                                               [136K]
 // with eps_i = e^{G_last - G_i} for the chunk's valid rows, 0 past them.
-constexpr size_t kWsMc0 = 0, kWsMc1 = 16384, kWsEc = 32768;
-constexpr size_t kWsQc0 = 49152, kWsQc1 = 57344, kWsFc = 65536;
-constexpr size_t kWsV = 73728, kWsS = 90112, kWsScal = 122880;
+constexpr size_t kWsMc0 = 0, kWsMc1 = 16384, kWsBc = 32768;
+constexpr size_t kWsQc0 = 65536, kWsQc1 = 73728, kWsFc = 81920;
+constexpr size_t kWsV = 90112, kWsS = 106496, kWsScal = 139264;
 constexpr size_t kVBytes = 16384, kSBytes = 32768;
-constexpr size_t kPerVHead = 123904;
+constexpr size_t kPerVHead = 140288;
 
 inline int prefill_max_chunks(int num_seqs, int total_tokens)
 {

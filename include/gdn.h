@@ -110,7 +110,7 @@ gdn_status_t gdn_prefill(const gdn_shape_t *shape,
  *
  * Arguments and results are those of gdn_prefill without the workspace: the
  * scratch lives in a fixed 64 MiB array of device memory that the library
- * holds on every GPU that loads it, until the process exits (about 1,000
+ * holds on every GPU that loads it, until the process exits (about 850
  * packed tokens at Hv = 32).  A shape whose
  * gdn_prefill_workspace_bytes exceeds 64 MiB returns GDN_ERR_WORKSPACE
  * before any launch.  Nothing in the array needs clearing between calls.
