@@ -113,6 +113,8 @@ out_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_z, const __grid
     }
     __syncthreads();
     tc_fence_after();
+    // launched early behind the scan kernel: its S copies are read below
+    grid_dep_wait();
     const uint32_t tbase = s->tmem_base;
     // Every role walks the same units (u = chunk * Hv + head, strided by the
     // grid) and counts only the live ones, so stage k % 2 and barrier phases
@@ -307,11 +309,20 @@ cudaError_t launch_prefill_out(const PrefillArgs &p, cudaStream_t stream)
             return e;
     }
     const int units = p.max_chunks * p.hv;
-    const dim3 grid(units < sm_count[dev] ? units : sm_count[dev]);
-    if (p.z)
-        out_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(p, tz, to);
-    else
-        out_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(p, tz, to);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(units < sm_count[dev] ? units : sm_count[dev]);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = p.z ? cudaLaunchKernelEx(&cfg, out_kernel<true>, p, tz, to)
+                        : cudaLaunchKernelEx(&cfg, out_kernel<false>, p, tz, to);
+    if (e != cudaSuccess)
+        return e;
     return cudaGetLastError();
 }
 

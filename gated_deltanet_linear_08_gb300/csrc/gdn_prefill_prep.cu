@@ -653,6 +653,7 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
         bulk_s2g(ws + kWsMc0, sm + kOffStMc, 32768);
         bulk_wait_all();
     }
+    grid_dep_launch();   // the scan kernel may start launching
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(s->tmem_base, kTmemCols);

@@ -157,6 +157,8 @@ scan_kernel(PrefillArgs p)
     }
     __syncthreads();
     tc_fence_after();
+    // launched early behind the prep kernel: its records are read below
+    grid_dep_wait();
     const uint32_t tbase = s->tmem_base;
     const uint32_t idesc = make_idesc_f16(128, kNv, false, true);
 
@@ -285,6 +287,7 @@ scan_kernel(PrefillArgs p)
             reinterpret_cast<float4 *>(p.final_state + sidx)[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
     }
 
+    grid_dep_launch();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -304,9 +307,17 @@ cudaError_t launch_prefill_scan(const PrefillArgs &p, cudaStream_t stream)
             return e;
         configured = true;
     }
-    dim3 grid(kTiles, p.hv, p.num_seqs);
-    scan_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kTiles, p.hv, p.num_seqs);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, scan_kernel, p);
 }
 
 }  // namespace gdn

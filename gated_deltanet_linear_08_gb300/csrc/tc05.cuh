@@ -360,6 +360,14 @@ __device__ __forceinline__ void tma_store_3d(const void *tmap, int c0, int c1, i
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before the previous kernel in the stream ends;
+// grid_dep_wait() blocks until that kernel has completed and its memory
+// operations are visible.  grid_dep_launch() lets the next such kernel
+// start launching once every CTA of this grid has called it or exited.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // Warp-level 16x16 fp16 products for block algebra that is too small for a
 // tcgen05 tile (16 x 16 x 16 blocks, latency-bound).  ldmatrix.x4 loads four
