@@ -29,8 +29,8 @@
  *   gdn_oracle_core          the definition, token by token;
  *   gdn_oracle_core_chunked  the chunked (WY/UT) algebra, chunk length C,
  *                            written from the token form (delta_i = U_i).
- * The first is the oracle; the second is checked against it and mirrors, in
- * plain fp64 loops, the algebra the GPU path runs.
+ * The first is the oracle; the second is checked against it, in plain fp64
+ * loops, as a second route through the chunked algebra.
  *
  * No fast-math; build with -ffp-contract=off so x86 and Arm agree.
  */
