@@ -34,8 +34,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from gated_deltanet_linear_08_gb300.inputs import (CASE_DECODE, CASE_T2048, DecodeCase,  # noqa: E402
-                                                   PrefillCase, make_decode_inputs,
-                                                   make_prefill_inputs)
+                                                   DecodeSlotsCase, PrefillCase, make_decode_inputs,
+                                                   make_decode_slots_inputs, make_prefill_inputs)
 
 METRIC = "GDN prefill tokens/s & decode GB/s at Hv=32,D=128; % of tensor/HBM roofline"
 PREFILL_FLOP_PER_TOKEN_HEAD = 10 * 64 * 128 + 6 * 128 * 128   # 180,224 (C=64 chunked count)
@@ -301,12 +301,37 @@ def _oracle_decode_sample(B: int):
     return run
 
 
-def decode_state_bytes(batch: int, hv: int = 32, hk: int = 16) -> int:
-    """Algorithmic bytes of one decode step: every fp32 state read and written
-    once, plus the token inputs and the bf16 output."""
+def decode_state_bytes(batch: int, hv: int = 32, hk: int = 16, tokens: int = 1) -> int:
+    """Algorithmic bytes of one decode call: every fp32 state read and written
+    once, plus each token's inputs and bf16 output."""
     state = batch * hv * 128 * 128 * 4 * 2
-    io = batch * (2 * hk * 128 * 2 + hv * 128 * 2 + 2 * hv * 2 + hv * 128 * 2)
+    io = tokens * batch * (2 * hk * 128 * 2 + hv * 128 * 2 + 2 * hv * 2 + hv * 128 * 2)
     return state + io
+
+
+SLOTS_CASE = DecodeSlotsCase("decode_slots_B256_T4", batch=256, tokens=4, slots=256)
+
+
+def decode_slots_region(gdn, dev, stream, calls: int = 50, warmup: int = 5):
+    """Multi-token decode over a slot pool (256 sequences x 4 draft tokens, a
+    random slot permutation of a 256-slot pool): device time per call."""
+    y = make_decode_slots_inputs(SLOTS_CASE)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in y.items()}
+    out = torch.empty(SLOTS_CASE.batch, SLOTS_CASE.tokens, SLOTS_CASE.hv, 128, dtype=torch.bfloat16, device=dev)
+
+    def call():
+        gdn.decode_slots(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["pool"],
+                         state_idx=d["state_idx"], out=out, stream=stream)
+    for _ in range(warmup):
+        call()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(calls):
+        call()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / calls
 
 
 def cpu_baseline():
@@ -444,6 +469,13 @@ def main():
         "gpu_launches": 4 * args.steps,
         "clocks": clk.summary(),
     }
+    sl_ms = max_over_ranks(decode_slots_region(gdn, dev, stream), world)
+    sl_bytes = decode_state_bytes(SLOTS_CASE.batch, tokens=SLOTS_CASE.tokens)
+    line["decode_slots"] = {
+        "workload": "256 sequences x 4 draft tokens against a 256-slot state pool (random slot permutation)",
+        "value": world * sl_bytes / (sl_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_call": sl_ms,
+        "tokens_per_s": world * SLOTS_CASE.batch * SLOTS_CASE.tokens / (sl_ms * 1e-3),
+        "hbm_frac": sl_bytes / (sl_ms * 1e-3) / 1e9 / peaks["hbm"]}
     if not args.no_e2e:
         e2e_ms, h2d, d2h = e2e_region(gdn, x, dec_y, dev, max(10, min(args.steps, 200)),
                                       3, stream)

@@ -25,7 +25,7 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED",
                 3: "GDN_ERR_ALIGNMENT", 4: "GDN_ERR_CUDA", 5: "GDN_ERR_DEVICE_STATUS",
                 6: "GDN_ERR_WORKSPACE"}
 EXPORTED = ("gdn_status_string", "gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_decode",
-            "gdn_check_device_status", "gdn_prefill_noalloc")
+            "gdn_check_device_status", "gdn_prefill_noalloc", "gdn_decode_slots")
 
 
 class GdnError(RuntimeError):
@@ -65,6 +65,9 @@ def load(path: Optional[str] = None):
             lib.gdn_prefill_noalloc.argtypes = [ctypes.POINTER(Shape), P, P, P, P, P, P, P, P, P,
                                                 P, P, f32, P, P, P]
             lib.gdn_prefill_noalloc.restype = ctypes.c_int
+            lib.gdn_decode_slots.argtypes = [ctypes.POINTER(Shape), ctypes.c_int32, ctypes.c_int32, P, P, P, P,
+                                             P, P, P, P, P, P, P, f32, P, P]
+            lib.gdn_decode_slots.restype = ctypes.c_int
             lib.gdn_check_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
             lib.gdn_check_device_status.restype = ctypes.c_int
             _lib = lib
@@ -192,6 +195,33 @@ def decode(q, k, v, a, b, A_log, dt_bias, state, z=None, norm_w=None, eps: float
         _ptr(dt_bias, f32, "dt_bias", dev), _ptr(state, f32, "state", dev),
         _ptr(z, bf, "z", dev), _ptr(norm_w, bf, "norm_w", dev), float(eps),
         _ptr(out, bf, "out", dev), _stream_handle(stream, dev))
+    _check(code)
+    return out
+
+
+def decode_slots(q, k, v, a, b, A_log, dt_bias, state_pool, state_idx=None, z=None, norm_w=None,
+                 eps: float = 1e-6, out=None, stream=None):
+    """``tokens`` consecutive tokens per sequence through ``gdn_decode_slots``;
+    the pool slots named by ``state_idx`` are updated in place.
+
+    q, k [B, T, Hk, 128] bf16; v [B, T, Hv, 128] bf16; a, b [B, T, Hv] bf16;
+    state_pool [P, Hv, 128, 128] fp32; state_idx [B] int32 (device) or None
+    for slot n; z [B, T, Hv, 128] bf16 and norm_w [128] bf16 for the gated
+    RMSNorm.  Returns out [B, T, Hv, 128] bf16.
+    """
+    dev = q.device
+    B, T, hk = q.shape[0], q.shape[1], q.shape[2]
+    hv = v.shape[2]
+    if out is None:
+        out = torch.empty(B, T, hv, 128, dtype=torch.bfloat16, device=dev)
+    bf, f32 = torch.bfloat16, torch.float32
+    shape = make_shape(B, B * T, hk, hv)
+    code = load().gdn_decode_slots(
+        ctypes.byref(shape), int(T), int(state_pool.shape[0]), _ptr(q, bf, "q", dev), _ptr(k, bf, "k", dev),
+        _ptr(v, bf, "v", dev), _ptr(a, bf, "a", dev), _ptr(b, bf, "b", dev), _ptr(A_log, f32, "A_log", dev),
+        _ptr(dt_bias, f32, "dt_bias", dev), _ptr(state_pool, f32, "state_pool", dev),
+        _ptr(state_idx, torch.int32, "state_idx", dev), _ptr(z, bf, "z", dev), _ptr(norm_w, bf, "norm_w", dev),
+        float(eps), _ptr(out, bf, "out", dev), _stream_handle(stream, dev))
     _check(code)
     return out
 

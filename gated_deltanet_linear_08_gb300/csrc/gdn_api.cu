@@ -147,6 +147,63 @@ gdn_status_t gdn_prefill(const gdn_shape_t *s, const void *q, const void *k, con
     return gdn::launch_prefill(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+gdn_status_t gdn_decode_slots(const gdn_shape_t *s, int32_t tokens, int32_t num_slots, const void *q,
+                              const void *k, const void *v, const void *a, const void *b, const float *A_log,
+                              const float *dt_bias, float *state, const int32_t *state_idx, const void *z,
+                              const void *norm_w, float eps, void *out, void *stream)
+{
+    gdn_status_t st = check_shape(s);
+    if (st != GDN_OK)
+        return st;
+    if (tokens < 1 || tokens > 8 || num_slots < 0)
+        return GDN_ERR_INVALID_ARG;
+    if ((int64_t)s->total_tokens != (int64_t)s->num_seqs * tokens)
+        return GDN_ERR_INVALID_ARG;
+    const size_t B = (size_t)s->num_seqs;
+    if (B == 0)
+        return GDN_OK;
+    if (!state_idx && (size_t)num_slots < B)
+        return GDN_ERR_INVALID_ARG;
+    if (!q || !k || !v || !a || !b || !A_log || !dt_bias || !out || (num_slots > 0 && !state))
+        return GDN_ERR_INVALID_ARG;
+    if (z && !norm_w)
+        return GDN_ERR_INVALID_ARG;
+    if (!(eps >= 0.f))
+        return GDN_ERR_INVALID_ARG;
+    const void *al16[] = {q, k, v, a, b, state, z, norm_w, out};
+    for (const void *p : al16)
+        if (p && !aligned(p, 16))
+            return GDN_ERR_ALIGNMENT;
+    if (state_idx && !aligned(state_idx, 4))
+        return GDN_ERR_ALIGNMENT;
+    const size_t hk = s->hk, hv = s->hv, BT = B * (size_t)tokens;
+    const size_t out_b = BT * hv * 256;
+    const struct { const void *p; size_t n; } ins[] = {
+        {q, BT * hk * 256}, {k, BT * hk * 256}, {v, BT * hv * 256}, {a, BT * hv * 2},
+        {b, BT * hv * 2}, {z, z ? BT * hv * 256 : 0}, {state, (size_t)num_slots * hv * 128 * 128 * 4},
+        {state_idx, state_idx ? B * 4 : 0}};
+    for (const auto &x : ins)
+        if (overlaps(out, out_b, x.p, x.n))
+            return GDN_ERR_INVALID_ARG;
+
+    gdn::DecodeArgs p{};
+    p.batch = s->num_seqs;
+    p.hk = s->hk;
+    p.hv = s->hv;
+    p.tokens = tokens;
+    p.num_slots = num_slots;
+    p.state_idx = state_idx;
+    p.q = q; p.k = k; p.v = v; p.a = a; p.b = b;
+    p.A_log = A_log; p.dt_bias = dt_bias;
+    p.state = state;
+    p.z = z; p.norm_w = norm_w; p.eps = eps;
+    p.out = out;
+    p.status = status_ptr();
+    if (!p.status)
+        return GDN_ERR_CUDA;
+    return gdn::launch_decode(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 gdn_status_t gdn_decode(const gdn_shape_t *s, const void *q, const void *k, const void *v,
                         const void *a, const void *b, const float *A_log, const float *dt_bias,
                         float *state, const void *z, const void *norm_w, float eps, void *out,
@@ -157,41 +214,10 @@ gdn_status_t gdn_decode(const gdn_shape_t *s, const void *q, const void *k, cons
         return st;
     if (s->total_tokens != s->num_seqs)
         return GDN_ERR_INVALID_ARG;
-    const size_t B = (size_t)s->num_seqs;
-    if (B == 0)
-        return GDN_OK;
-    if (!q || !k || !v || !a || !b || !A_log || !dt_bias || !state || !out)
+    if (s->num_seqs > 0 && !state)
         return GDN_ERR_INVALID_ARG;
-    if (z && !norm_w)
-        return GDN_ERR_INVALID_ARG;
-    if (!(eps >= 0.f))
-        return GDN_ERR_INVALID_ARG;
-    const void *al16[] = {q, k, v, a, b, state, z, norm_w, out};
-    for (const void *p : al16)
-        if (p && !aligned(p, 16))
-            return GDN_ERR_ALIGNMENT;
-    const size_t hk = s->hk, hv = s->hv;
-    const size_t out_b = B * hv * 256;
-    const struct { const void *p; size_t n; } ins[] = {
-        {q, B * hk * 256}, {k, B * hk * 256}, {v, B * hv * 256}, {a, B * hv * 2},
-        {b, B * hv * 2}, {z, z ? B * hv * 256 : 0}, {state, B * hv * 128 * 128 * 4}};
-    for (const auto &x : ins)
-        if (overlaps(out, out_b, x.p, x.n))
-            return GDN_ERR_INVALID_ARG;
-
-    gdn::DecodeArgs p{};
-    p.batch = s->num_seqs;
-    p.hk = s->hk;
-    p.hv = s->hv;
-    p.q = q; p.k = k; p.v = v; p.a = a; p.b = b;
-    p.A_log = A_log; p.dt_bias = dt_bias;
-    p.state = state;
-    p.z = z; p.norm_w = norm_w; p.eps = eps;
-    p.out = out;
-    p.status = status_ptr();
-    if (!p.status)
-        return GDN_ERR_CUDA;
-    return gdn::launch_decode(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    return gdn_decode_slots(s, 1, s->num_seqs, q, k, v, a, b, A_log, dt_bias, state, nullptr, z, norm_w,
+                            eps, out, stream);
 }
 
 gdn_status_t gdn_check_device_status(uint32_t *bits)

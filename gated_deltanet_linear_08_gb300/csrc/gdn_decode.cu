@@ -1,19 +1,20 @@
-// gdn_decode.cu -- single-token GDN decode with the fp32 state updated in
-// place (the per-request recurrent-state slots of serving: SGLang page
-// "[Perf] Pack the Qwen3.5 GDN input projection on CUDA", Accuracy Tests,
-// "16 mamba slots").
+// gdn_decode.cu -- GDN decode with the fp32 state updated in place: one
+// token per sequence, or a few consecutive tokens (a speculative draft),
+// against a pool of recurrent-state slots (the per-request state slots of
+// serving: SGLang page "[Perf] Pack the Qwen3.5 GDN input projection on
+// CUDA", Accuracy Tests, "16 mamba slots").
 //
 // One CTA per (sequence, value head) streams its 128x128 fp32 state (64 KB)
 // exactly once: every thread keeps 16 rows x 4 columns of the state in
-// registers between the read and the write.  The update needs
+// registers from the read, through every token, to the write.  Per token
 //   r_k = S_old^T kn,  r_q = S_old^T qn          (reductions over Dk)
 //   delta = beta (v - e^g r_k)
 //   o = scale (e^g r_q + (kn . qn) delta)        (= scale * S_new^T qn)
 //   S_new = e^g S_old + kn delta^T
-// so both reductions come from the old state in the same pass and the write
-// follows once delta is known.  The path is HBM-bound (about 7 flop per 8
-// bytes of state): loads and stores are 16-byte, warp-contiguous rows of 512
-// bytes, marked streaming so they do not displace other data in L2.
+// so both reductions come from the old state and the update needs no second
+// pass.  The path is HBM-bound (about 7 flop per 8 bytes of state for one
+// token): loads and stores are 16-byte, warp-contiguous rows of 512 bytes,
+// marked streaming so they do not displace other data in L2.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -29,7 +30,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 decode_kernel(DecodeArgs p)
 {
     const int h = blockIdx.x, n = blockIdx.y;
-    const int hv = p.hv, hk = p.hk;
+    const int hv = p.hv, hk = p.hk, T = p.tokens;
     const int hq = h / (hv / hk);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -38,7 +39,23 @@ decode_kernel(DecodeArgs p)
     __shared__ float s_scal[4];   // e^g, beta, kn.qn
     __shared__ float s_red[4];
 
-    float *S = p.state + ((size_t)n * hv + h) * (size_t)(kD * kD);
+    __nv_bfloat16 *outg = reinterpret_cast<__nv_bfloat16 *>(p.out);
+    int slot = n;
+    if (p.state_idx) {
+        slot = p.state_idx[n];
+        if (slot >= p.num_slots) {   // out of the pool: flagged and skipped
+            if (tid == 0)
+                set_status(p.status, kStatusRange);
+            slot = -1;
+        }
+    }
+    if (slot < 0) {   // no state for this sequence: zero outputs
+        if (tid < kD)
+            for (int t = 0; t < T; ++t)
+                outg[(((size_t)n * T + t) * hv + h) * kD + tid] = __float2bfloat16_rn(0.f);
+        return;
+    }
+    float *S = p.state + ((size_t)slot * hv + h) * (size_t)(kD * kD);
 
     // 1. Issue every state load first so the whole 64 KB is in flight.
     float4 st[kRowsPerThread];
@@ -46,116 +63,121 @@ decode_kernel(DecodeArgs p)
     for (int i = 0; i < kRowsPerThread; ++i)
         st[i] = __ldcs(reinterpret_cast<const float4 *>(S + (size_t)(warp + kWarps * i) * kD) + lane);
 
-    // 2. Per-token inputs: warp 0 normalises k, warp 1 q, warp 2 loads v,
-    //    warp 3 computes the gate and beta.
-    if (warp < 2) {
-        const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(warp == 0 ? p.k : p.q)
-                                   + ((size_t)n * hk + hq) * kD + lane * 4;
-        const uint2 u = *reinterpret_cast<const uint2 *>(src);
-        float f[4] = {__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
-                      __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u)};
-        float ss = f[0] * f[0] + f[1] * f[1] + f[2] * f[2] + f[3] * f[3];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        const float r = 1.f / sqrtf(ss + kL2Eps);
-        float *dst = warp == 0 ? s_k : s_q;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            dst[lane * 4 + j] = f[j] * r;
-    } else if (warp == 2) {
-        const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(p.v)
-                                   + ((size_t)n * hv + h) * kD + lane * 4;
-        const uint2 u = *reinterpret_cast<const uint2 *>(src);
-        s_v[lane * 4 + 0] = __uint_as_float(u.x << 16);
-        s_v[lane * 4 + 1] = __uint_as_float(u.x & 0xFFFF0000u);
-        s_v[lane * 4 + 2] = __uint_as_float(u.y << 16);
-        s_v[lane * 4 + 3] = __uint_as_float(u.y & 0xFFFF0000u);
-    } else if (warp == 3 && lane == 0) {
-        const float av = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.a)[(size_t)n * hv + h]);
-        const float bv = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.b)[(size_t)n * hv + h]);
-        s_scal[0] = expf(gate_f(av, p.A_log[h], p.dt_bias[h]));
-        s_scal[1] = sigmoid_f(bv);
-    }
-    __syncthreads();
-
-    // 3. Partial reductions over this thread's 16 rows, for 4 columns.
-    float rk[4] = {0.f, 0.f, 0.f, 0.f}, rq[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int i = 0; i < kRowsPerThread; ++i) {
-        const int r = warp + kWarps * i;
-        const float kk = s_k[r], qq = s_q[r];
-        rk[0] = fmaf(st[i].x, kk, rk[0]); rq[0] = fmaf(st[i].x, qq, rq[0]);
-        rk[1] = fmaf(st[i].y, kk, rk[1]); rq[1] = fmaf(st[i].y, qq, rq[1]);
-        rk[2] = fmaf(st[i].z, kk, rk[2]); rq[2] = fmaf(st[i].z, qq, rq[2]);
-        rk[3] = fmaf(st[i].w, kk, rk[3]); rq[3] = fmaf(st[i].w, qq, rq[3]);
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        s_part[0][warp][lane * 4 + j] = rk[j];
-        s_part[1][warp][lane * 4 + j] = rq[j];
-    }
-    if (warp == 0) {
-        float kq = 0.f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            kq = fmaf(s_k[lane * 4 + j], s_q[lane * 4 + j], kq);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            kq += __shfl_xor_sync(0xffffffffu, kq, o);
-        if (lane == 0)
-            s_scal[2] = kq;
-    }
-    __syncthreads();
-
-    // 4. Column c = tid (< 128): delta and the output.
-    const float eg = s_scal[0], beta = s_scal[1];
     const float scale = rsqrtf((float)kD);
-    float o = 0.f;
-    if (tid < kD) {
-        float sk = 0.f, sq = 0.f;
+    for (int t = 0; t < T; ++t) {
+        const size_t tok = (size_t)n * T + t;
+        // 2. Per-token inputs: warp 0 normalises k, warp 1 q, warp 2 loads v,
+        //    warp 3 computes the gate and beta.
+        if (warp < 2) {
+            const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(warp == 0 ? p.k : p.q)
+                                       + (tok * hk + hq) * kD + lane * 4;
+            const uint2 u = *reinterpret_cast<const uint2 *>(src);
+            float f[4] = {__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                          __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u)};
+            float ss = f[0] * f[0] + f[1] * f[1] + f[2] * f[2] + f[3] * f[3];
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            sk += s_part[0][w][tid];
-            sq += s_part[1][w][tid];
+            for (int o = 16; o > 0; o >>= 1)
+                ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            const float r = 1.f / sqrtf(ss + kL2Eps);
+            float *dst = warp == 0 ? s_k : s_q;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                dst[lane * 4 + j] = f[j] * r;
+        } else if (warp == 2) {
+            const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(p.v) + (tok * hv + h) * kD + lane * 4;
+            const uint2 u = *reinterpret_cast<const uint2 *>(src);
+            s_v[lane * 4 + 0] = __uint_as_float(u.x << 16);
+            s_v[lane * 4 + 1] = __uint_as_float(u.x & 0xFFFF0000u);
+            s_v[lane * 4 + 2] = __uint_as_float(u.y << 16);
+            s_v[lane * 4 + 3] = __uint_as_float(u.y & 0xFFFF0000u);
+        } else if (warp == 3 && lane == 0) {
+            const float av = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.a)[tok * hv + h]);
+            const float bv = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.b)[tok * hv + h]);
+            s_scal[0] = expf(gate_f(av, p.A_log[h], p.dt_bias[h]));
+            s_scal[1] = sigmoid_f(bv);
         }
-        const float delta = beta * (s_v[tid] - eg * sk);
-        s_delta[tid] = delta;
-        o = scale * (eg * sq + s_scal[2] * delta);
-        if (kNorm) {
-            float ss = o * o;
+        __syncthreads();
+
+        // 3. Partial reductions over this thread's 16 rows, for 4 columns.
+        float rk[4] = {0.f, 0.f, 0.f, 0.f}, rq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-                ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        for (int i = 0; i < kRowsPerThread; ++i) {
+            const int r = warp + kWarps * i;
+            const float kk = s_k[r], qq = s_q[r];
+            rk[0] = fmaf(st[i].x, kk, rk[0]); rq[0] = fmaf(st[i].x, qq, rq[0]);
+            rk[1] = fmaf(st[i].y, kk, rk[1]); rq[1] = fmaf(st[i].y, qq, rq[1]);
+            rk[2] = fmaf(st[i].z, kk, rk[2]); rq[2] = fmaf(st[i].z, qq, rq[2]);
+            rk[3] = fmaf(st[i].w, kk, rk[3]); rq[3] = fmaf(st[i].w, qq, rq[3]);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            s_part[0][warp][lane * 4 + j] = rk[j];
+            s_part[1][warp][lane * 4 + j] = rq[j];
+        }
+        if (warp == 0) {
+            float kq = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                kq = fmaf(s_k[lane * 4 + j], s_q[lane * 4 + j], kq);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                kq += __shfl_xor_sync(0xffffffffu, kq, o);
             if (lane == 0)
-                s_red[warp] = ss;
+                s_scal[2] = kq;
         }
-    }
-    __syncthreads();
-    if (tid < kD) {
-        __nv_bfloat16 *outp = reinterpret_cast<__nv_bfloat16 *>(p.out) + ((size_t)n * hv + h) * kD;
-        if (kNorm) {
-            const float ms = (s_red[0] + s_red[1] + s_red[2] + s_red[3]) * (1.f / kD);
-            const float zz = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.z)[((size_t)n * hv + h) * kD + tid]);
-            const float ww = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.norm_w)[tid]);
-            o = o * rsqrtf(ms + p.eps) * ww * (zz * sigmoid_f(zz));
+        __syncthreads();
+
+        // 4. Column c = tid (< 128): delta and the output.
+        const float eg = s_scal[0], beta = s_scal[1];
+        float o = 0.f;
+        if (tid < kD) {
+            float sk = 0.f, sq = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                sk += s_part[0][w][tid];
+                sq += s_part[1][w][tid];
+            }
+            const float delta = beta * (s_v[tid] - eg * sk);
+            s_delta[tid] = delta;
+            o = scale * (eg * sq + s_scal[2] * delta);
+            if (kNorm) {
+                float ss = o * o;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1)
+                    ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                if (lane == 0)
+                    s_red[warp] = ss;
+            }
         }
-        outp[tid] = __float2bfloat16_rn(o);
+        __syncthreads();
+        if (tid < kD) {
+            if (kNorm) {
+                const float ms = (s_red[0] + s_red[1] + s_red[2] + s_red[3]) * (1.f / kD);
+                const float zz = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.z)[(tok * hv + h) * kD + tid]);
+                const float ww = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.norm_w)[tid]);
+                o = o * rsqrtf(ms + p.eps) * ww * (zz * sigmoid_f(zz));
+            }
+            outg[(tok * hv + h) * kD + tid] = __float2bfloat16_rn(o);
+        }
+
+        // 5. S_new = e^g S_old + kn delta^T, kept in registers.
+        const float4 d4 = *reinterpret_cast<const float4 *>(&s_delta[lane * 4]);
+#pragma unroll
+        for (int i = 0; i < kRowsPerThread; ++i) {
+            const float kk = s_k[warp + kWarps * i];
+            st[i].x = fmaf(eg, st[i].x, kk * d4.x);
+            st[i].y = fmaf(eg, st[i].y, kk * d4.y);
+            st[i].z = fmaf(eg, st[i].z, kk * d4.z);
+            st[i].w = fmaf(eg, st[i].w, kk * d4.w);
+        }
+        if (t + 1 < T)
+            __syncthreads();   // the next token overwrites the shared inputs
     }
 
-    // 5. S_new = e^g S_old + kn delta^T, written back in place.
-    const float4 d4 = *reinterpret_cast<const float4 *>(&s_delta[lane * 4]);
+    // 6. Written back in place, once.
 #pragma unroll
-    for (int i = 0; i < kRowsPerThread; ++i) {
-        const int r = warp + kWarps * i;
-        const float kk = s_k[r];
-        float4 x = st[i];
-        x.x = fmaf(eg, x.x, kk * d4.x);
-        x.y = fmaf(eg, x.y, kk * d4.y);
-        x.z = fmaf(eg, x.z, kk * d4.z);
-        x.w = fmaf(eg, x.w, kk * d4.w);
-        __stcs(reinterpret_cast<float4 *>(S + (size_t)r * kD) + lane, x);
-    }
+    for (int i = 0; i < kRowsPerThread; ++i)
+        __stcs(reinterpret_cast<float4 *>(S + (size_t)(warp + kWarps * i) * kD) + lane, st[i]);
 }
 
 }  // namespace

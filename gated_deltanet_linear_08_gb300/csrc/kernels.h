@@ -11,9 +11,12 @@ namespace gdn {
 
 struct DecodeArgs {
     int batch, hk, hv;
+    int tokens;                    // consecutive tokens per sequence (1..8)
+    int num_slots;                 // slots in the state pool
+    const int32_t *state_idx;      // slot per sequence, or null for slot n
     const void *q, *k, *v, *a, *b;
     const float *A_log, *dt_bias;
-    float *state;
+    float *state;                  // state pool [num_slots, hv, 128, 128]
     const void *z, *norm_w;
     float eps;
     void *out;

@@ -66,6 +66,27 @@ class DecodeCase:
     seed: int = 0
 
 
+@dataclass
+class DecodeSlotsCase:
+    """Decode of ``tokens`` consecutive tokens per sequence against a pool of
+    ``slots`` recurrent states.  Sequence n uses a distinct random slot;
+    ``skipped`` of them carry slot -1 and ``out_of_pool`` carry slot ``slots``
+    (past the pool)."""
+
+    name: str
+    batch: int = 64
+    tokens: int = 4
+    slots: int = 96
+    skipped: int = 0
+    out_of_pool: int = 0
+    hk: int = 16
+    hv: int = 32
+    d: int = D_HEAD
+    gated_norm: bool = False
+    eps: float = 1e-6
+    seed: int = 0
+
+
 def _bf16(x: torch.Tensor) -> torch.Tensor:
     return x.to(torch.bfloat16)
 
@@ -133,6 +154,33 @@ def make_decode_inputs(case: DecodeCase) -> dict:
         w = _bf16(1.0 + 0.1 * torch.randn(d, generator=g))
     return dict(A_log=A_log, dt_bias=dt_bias, state=state, steps=steps, z=z,
                 norm_w=w, eps=case.eps, hk=hk, hv=hv, d=d, batch=B)
+
+
+def make_decode_slots_inputs(case: DecodeSlotsCase) -> dict:
+    """Return CPU tensors for a slot-pool decode case.  Draw order: A_log,
+    dt_bias, the pool, the slot permutation, the skipped and out-of-pool
+    sequences, q, k, v, a, b, then z and w."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(case.seed)
+    B, T, P, hk, hv, d = case.batch, case.tokens, case.slots, case.hk, case.hv, case.d
+    A_log = torch.log(torch.empty(hv).uniform_(1.0, 16.0, generator=g)).float()
+    dt_bias = torch.randn(hv, generator=g).float()
+    pool = (torch.randn(P, hv, d, d, generator=g) * 0.1).float()
+    idx = torch.randperm(P, generator=g)[:B].to(torch.int32)
+    pick = torch.randperm(B, generator=g)
+    idx[pick[:case.skipped]] = -1
+    idx[pick[case.skipped:case.skipped + case.out_of_pool]] = P
+    q = _bf16(torch.randn(B, T, hk, d, generator=g))
+    k = _bf16(torch.randn(B, T, hk, d, generator=g))
+    v = _bf16(torch.randn(B, T, hv, d, generator=g))
+    a = _bf16(torch.randn(B, T, hv, generator=g))
+    b = _bf16(torch.randn(B, T, hv, generator=g))
+    z = w = None
+    if case.gated_norm:
+        z = _bf16(torch.randn(B, T, hv, d, generator=g))
+        w = _bf16(1.0 + 0.1 * torch.randn(d, generator=g))
+    return dict(q=q, k=k, v=v, a=a, b=b, A_log=A_log, dt_bias=dt_bias, pool=pool, state_idx=idx,
+                z=z, norm_w=w, eps=case.eps, hk=hk, hv=hv, d=d, batch=B, tokens=T, slots=P)
 
 
 # The workloads of the contract: the Qwen3.5-4B geometry (16/16/32/128) at

@@ -150,6 +150,40 @@ gdn_status_t gdn_decode(const gdn_shape_t *shape,
                         const void *z, const void *norm_w, float eps,
                         void *out, void *stream);
 
+/*
+ * gdn_decode_slots -- decode of `tokens` consecutive tokens per sequence
+ * (1 <= tokens <= 8: a single step, or a short draft verified together)
+ * against a pool of recurrent-state slots (SGLang page "[Perf] Pack the
+ * Qwen3.5 GDN input projection on CUDA", Accuracy Tests: mamba slots).
+ * Each sequence's state is read once, advanced through its tokens in order
+ * exactly as the recurrence of gdn_decode would advance it token by token,
+ * and written back once, in place.
+ *
+ *   shape->num_seqs = B; shape->total_tokens must equal B * tokens.
+ *   q, k     bf16 [B, tokens, Hk, 128];  v bf16 [B, tokens, Hv, 128]
+ *   a, b     bf16 [B, tokens, Hv]
+ *   A_log, dt_bias fp32 [Hv]
+ *   state_pool fp32 [num_slots, Hv, 128, 128]; sequence n uses slot
+ *            state_idx[n] (int32 [B] on the device), or slot n when
+ *            state_idx is NULL (then num_slots must be >= B).  A negative
+ *            index skips the sequence: its outputs are zero and no state is
+ *            touched.  An index >= num_slots is skipped the same way and
+ *            sets the range bit of the device status word.  Sequences must
+ *            name distinct slots; two sequences on one slot race.
+ *   z        bf16 [B, tokens, Hv, 128] or NULL (no epilogue); norm_w, eps
+ *            as gdn_decode
+ *   out      bf16 [B, tokens, Hv, 128]; must not overlap any input or the pool
+ * gdn_decode(shape, ...) is gdn_decode_slots with tokens = 1, no index and
+ * num_slots = B.
+ */
+gdn_status_t gdn_decode_slots(const gdn_shape_t *shape, int32_t tokens, int32_t num_slots,
+                              const void *q, const void *k, const void *v,
+                              const void *a, const void *b,
+                              const float *A_log, const float *dt_bias,
+                              float *state_pool, const int32_t *state_idx,
+                              const void *z, const void *norm_w, float eps,
+                              void *out, void *stream);
+
 /* Reads and clears the device status word that kernels set when a bounded
  * wait runs out.  Synchronises the device: not for the hot path.  Returns
  * GDN_OK, GDN_ERR_DEVICE_STATUS (and the raw bits in *bits when non-NULL),

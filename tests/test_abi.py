@@ -109,6 +109,28 @@ def test_decode_rejects_bad_arguments(lib):
     assert dec(B.make_shape(0, 0, 16, 32)) == 0
 
 
+def test_decode_slots_rejects_bad_arguments(lib):
+    # host-side validation only: every call here fails before any launch
+    def dec(shape, tokens=2, slots=8, **kw):
+        a = dict(q=FAKE, k=FAKE + 0x10000000, v=FAKE + 0x20000000, a=FAKE + 0x30000000,
+                 b=FAKE + 0x40000000, A_log=FAKE + 0x50000000, dt=FAKE + 0x60000000,
+                 state=FAKE + 0x70000000, idx=FAKE + 0x80000000, z=None, w=None, eps=1e-6,
+                 out=FAKE + 0x90000000)
+        a.update(kw)
+        return lib.gdn_decode_slots(ctypes.byref(shape), tokens, slots, a["q"], a["k"], a["v"], a["a"],
+                                    a["b"], a["A_log"], a["dt"], a["state"], a["idx"], a["z"], a["w"],
+                                    a["eps"], a["out"], None)
+    assert dec(B.make_shape(4, 8, 16, 32), tokens=0) == 1         # tokens outside 1..8
+    assert dec(B.make_shape(4, 36, 16, 32), tokens=9) == 1
+    assert dec(B.make_shape(4, 7, 16, 32)) == 1                   # total_tokens != B * tokens
+    assert dec(B.make_shape(4, 8, 16, 32), slots=-1) == 1
+    assert dec(B.make_shape(4, 8, 16, 32), slots=3, idx=None) == 1   # identity slots need P >= B
+    assert dec(B.make_shape(4, 8, 16, 32), idx=FAKE + 0x80000000 + 2) == 3   # index not 4-byte aligned
+    assert dec(B.make_shape(4, 8, 16, 32), out=FAKE + 0x70000000) == 1       # out overlaps the pool
+    assert dec(B.make_shape(4, 8, 16, 32, dv=64)) == 2
+    assert dec(B.make_shape(0, 0, 16, 32)) == 0                   # empty batch: no-op
+
+
 def test_missing_library_fails_loudly(tmp_path):
     saved = B._lib
     try:

@@ -325,3 +325,23 @@ def test_decode_step_equals_one_token_prefill_and_one_pass_identity():
             np.testing.assert_allclose(out[n, h], o1, rtol=0, atol=1e-14)
             np.testing.assert_allclose(S[n, h], eg * S_old[n, h] + np.outer(kn[n, hq], delta),
                                        rtol=0, atol=1e-15)
+
+
+def test_multi_token_decode_equals_recurrence_over_the_draft():
+    """Decoding T tokens of one sequence in a row (a speculative draft) is the
+    recurrence over those T tokens from the sequence's state: T successive
+    oracle decode steps equal the token-by-token core over a T-token sequence
+    with that initial state, outputs and final state."""
+    T, hk, hv, dk = 5, 2, 4, 128
+    q = RNG.standard_normal((T, hk, dk)); k = RNG.standard_normal((T, hk, dk))
+    v = RNG.standard_normal((T, hv, dk))
+    a = RNG.standard_normal((T, hv)); b = RNG.standard_normal((T, hv))
+    A_log = np.log(RNG.uniform(1, 16, hv)); dt_bias = RNG.standard_normal(hv)
+    S0 = 0.1 * RNG.standard_normal((1, hv, dk, dk))
+    S = S0.copy()
+    outs = [oracle.decode_step(q[t:t + 1], k[t:t + 1], v[t:t + 1], a[t:t + 1], b[t:t + 1],
+                               A_log, dt_bias, S)[0] for t in range(T)]
+    g, beta, qn, kn = oracle.prep(q, k, a, b, A_log, dt_bias)
+    o2, f2 = oracle.core(np.array([0, T], np.int32), g, beta, qn, kn, v, S0)
+    np.testing.assert_allclose(np.stack(outs), o2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(S, f2, rtol=0, atol=1e-13)
