@@ -1,0 +1,111 @@
+"""Serving-style integration of the path on the GPU (pegainfer page
+"feat(qwen35): add SM120 FlashInfer GDN prefill candidate", Correctness:
+chunked vs unchunked prefill with carried states; SGLang page "[Perf] Pack
+the Qwen3.5 GDN input projection on CUDA", Accuracy Tests: mamba slots and
+graph-captured decode).
+
+  * prefill in 512-token pieces per call, several sequences at once, each
+    call starting from the states the previous call returned, equals one
+    call over the whole sequences bit for bit: piece boundaries are chunk
+    boundaries, so every chunk sees the same tokens and the same fp32 state;
+  * a decode loop over a slot pool captured in a CUDA graph and replayed
+    equals the same calls made eagerly, bit for bit;
+  * a captured prefill call equals the eager call.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gated_deltanet_linear_08_gb300.inputs import (DecodeSlotsCase, PrefillCase, make_decode_slots_inputs,
+                                                   make_prefill_inputs)
+from parity_util import to_dev
+
+pytestmark = pytest.mark.gpu
+PIECE = 512
+
+
+def test_prefill_in_pieces_with_carried_states_matches_one_call():
+    import gated_deltanet_linear_08_gb300 as gdn
+    lens = [700, 1300, 64, 2000, 1]
+    x = make_prefill_inputs(PrefillCase("pieces", seqlens=lens, hk=4, hv=8, init_state=True,
+                                        gated_norm=True, seed=21))
+    d = to_dev(x)
+    full_out, full_fin = gdn.prefill(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"],
+                                     d["cu_seqlens"], init_state=d["init_state"], z=d["z"],
+                                     norm_w=d["norm_w"], eps=x["eps"])
+    starts = np.concatenate([[0], np.cumsum(lens)])
+    states = d["init_state"].clone()
+    out = torch.zeros_like(full_out)
+    for i in range(max(lens) // PIECE + 1):
+        live = [n for n in range(len(lens)) if lens[n] > PIECE * i]
+        rows = [np.arange(starts[n] + PIECE * i, starts[n] + min(PIECE * (i + 1), lens[n])) for n in live]
+        sel = torch.as_tensor(np.concatenate(rows), device="cuda")
+        cu = torch.as_tensor(np.concatenate([[0], np.cumsum([len(r) for r in rows])]), dtype=torch.int32,
+                             device="cuda")
+        pick = lambda t: t.index_select(0, sel).contiguous()
+        idx = torch.as_tensor(live, device="cuda")
+        o, fin = gdn.prefill(pick(d["q"]), pick(d["k"]), pick(d["v"]), pick(d["a"]), pick(d["b"]),
+                             d["A_log"], d["dt_bias"], cu, init_state=states.index_select(0, idx).contiguous(),
+                             z=pick(d["z"]), norm_w=d["norm_w"], eps=x["eps"])
+        out.index_copy_(0, sel, o)
+        states.index_copy_(0, idx, fin)
+    torch.cuda.synchronize()
+    assert torch.equal(out, full_out)
+    assert torch.equal(states, full_fin)
+    assert gdn.check_device_status() == 0
+
+
+def test_graph_captured_decode_loop_matches_eager():
+    import gated_deltanet_linear_08_gb300 as gdn
+    case = DecodeSlotsCase("graph", batch=16, tokens=1, slots=40, skipped=2, hk=4, hv=8, seed=5)
+    steps = 12
+    ys = [make_decode_slots_inputs(DecodeSlotsCase(case.name, batch=case.batch, tokens=1, slots=case.slots,
+                                                   skipped=case.skipped, hk=case.hk, hv=case.hv, seed=100 + s))
+          for s in range(steps)]
+    base = make_decode_slots_inputs(case)
+    toks = [{n: y[n].cuda() for n in ("q", "k", "v", "a", "b")} for y in ys]
+    A_log, dt = base["A_log"].cuda(), base["dt_bias"].cuda()
+    idx = base["state_idx"].cuda()
+    outs_e = [torch.empty(case.batch, 1, case.hv, 128, dtype=torch.bfloat16, device="cuda") for _ in range(steps)]
+    outs_g = [torch.empty_like(o) for o in outs_e]
+
+    def loop(pool, outs, stream=None):
+        for s in range(steps):
+            t = toks[s]
+            gdn.decode_slots(t["q"], t["k"], t["v"], t["a"], t["b"], A_log, dt, pool, state_idx=idx,
+                             out=outs[s], stream=stream)
+
+    pool_e = base["pool"].cuda()
+    loop(pool_e, outs_e)   # eager (also the warm-up before capture)
+    pool_g = base["pool"].cuda()
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    pool_g0 = pool_g.clone()
+    with torch.cuda.graph(graph, stream=stream):
+        loop(pool_g, outs_g, stream=stream)
+    pool_g.copy_(pool_g0)   # capture runs nothing; start the replay from the initial pool
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(pool_g, pool_e)
+    assert all(torch.equal(a, b) for a, b in zip(outs_g, outs_e))
+    assert gdn.check_device_status() == 0
+
+
+def test_graph_captured_prefill_matches_eager():
+    import gated_deltanet_linear_08_gb300 as gdn
+    x = make_prefill_inputs(PrefillCase("gprefill", seqlens=[300, 65, 129], hk=2, hv=4, init_state=True,
+                                        gated_norm=True, seed=8))
+    d = to_dev(x)
+    ws = gdn.alloc_workspace(3, d["q"].shape[0], 2, 4, "cuda")
+    args = (d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["cu_seqlens"])
+    kw = dict(init_state=d["init_state"], z=d["z"], norm_w=d["norm_w"], eps=x["eps"], workspace=ws)
+    out_e, fin_e = gdn.prefill(*args, **kw)
+    out_g, fin_g = torch.empty_like(out_e), torch.empty_like(fin_e)
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        gdn.prefill(*args, **kw, out=out_g, final_state=fin_g, stream=stream)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out_g, out_e) and torch.equal(fin_g, fin_e)
+    assert gdn.check_device_status() == 0
