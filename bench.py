@@ -150,6 +150,34 @@ def build_prefill_sets(dev, case: PrefillCase, n_sets: int):
     return x, shared, sets
 
 
+def packed_prefill_region(gdn, pre, stream, calls: int = 30, warmup: int = 3):
+    """The T = 2048 prefill with q, k, v, z, b, a read in place from one packed
+    projection buffer [T, 12352] (row order q | k | v | z | b | a): device
+    time per call, rotating over the same number of buffer sets."""
+    x, shared, sets = pre
+    packed = []
+    for st in sets:
+        parts = [st["q"].flatten(1), st["k"].flatten(1), st["v"].flatten(1), st["z"].flatten(1), st["b"], st["a"]]
+        buf = torch.cat(parts, dim=1).contiguous()
+        offs, views = 0, {}
+        for name, part in zip(("q", "k", "v", "z", "b", "a"), parts):
+            views[name] = buf[:, offs:offs + part.shape[1]]
+            offs += part.shape[1]
+        for name in ("q", "k", "v", "z"):
+            views[name] = views[name].unflatten(1, st[name].shape[1:])
+        packed.append(dict(st, **views, buf=buf))
+    for i in range(warmup):
+        run_prefill(gdn, shared, packed[i % len(packed)], x["eps"], stream)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(calls):
+        run_prefill(gdn, shared, packed[i % len(packed)], x["eps"], stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / calls
+
+
 def run_prefill(gdn, shared, s, eps, stream):
     gdn.prefill(s["q"], s["k"], s["v"], s["a"], s["b"], shared["A_log"], shared["dt_bias"],
                 shared["cu_seqlens"], init_state=None, z=s["z"], norm_w=shared["norm_w"],
@@ -469,6 +497,10 @@ def main():
         "gpu_launches": 4 * args.steps,
         "clocks": clk.summary(),
     }
+    pk_ms = max_over_ranks(packed_prefill_region(gdn, pre, stream), world)
+    line["prefill_packed_inputs"] = {
+        "workload": "the same T=2048 prefill, inputs read in place from a packed [T, 12352] projection buffer",
+        "ms_per_call": pk_ms, "tokens_per_s": world * T / (pk_ms * 1e-3)}
     sl_ms = max_over_ranks(decode_slots_region(gdn, dev, stream), world)
     sl_bytes = decode_state_bytes(SLOTS_CASE.batch, tokens=SLOTS_CASE.tokens)
     line["decode_slots"] = {

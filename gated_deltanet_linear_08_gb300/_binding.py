@@ -25,7 +25,8 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED",
                 3: "GDN_ERR_ALIGNMENT", 4: "GDN_ERR_CUDA", 5: "GDN_ERR_DEVICE_STATUS",
                 6: "GDN_ERR_WORKSPACE"}
 EXPORTED = ("gdn_status_string", "gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_decode",
-            "gdn_check_device_status", "gdn_prefill_noalloc", "gdn_decode_slots")
+            "gdn_check_device_status", "gdn_prefill_noalloc", "gdn_decode_slots", "gdn_prefill_strided",
+            "gdn_decode_strided")
 
 
 class GdnError(RuntimeError):
@@ -38,6 +39,14 @@ class Shape(ctypes.Structure):
     _fields_ = [("num_seqs", ctypes.c_int32), ("total_tokens", ctypes.c_int32),
                 ("hq", ctypes.c_int32), ("hk", ctypes.c_int32), ("hv", ctypes.c_int32),
                 ("dk", ctypes.c_int32), ("dv", ctypes.c_int32)]
+
+
+class Stride(ctypes.Structure):
+    _fields_ = [("token", ctypes.c_int64), ("head", ctypes.c_int64)]
+
+
+class Strides(ctypes.Structure):
+    _fields_ = [("q", Stride), ("k", Stride), ("v", Stride), ("z", Stride), ("a", Stride), ("b", Stride)]
 
 
 def load(path: Optional[str] = None):
@@ -68,6 +77,12 @@ def load(path: Optional[str] = None):
             lib.gdn_decode_slots.argtypes = [ctypes.POINTER(Shape), ctypes.c_int32, ctypes.c_int32, P, P, P, P,
                                              P, P, P, P, P, P, P, f32, P, P]
             lib.gdn_decode_slots.restype = ctypes.c_int
+            lib.gdn_prefill_strided.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Strides), P, P, P, P, P, P,
+                                                P, P, P, P, P, f32, P, P, P, sz, P]
+            lib.gdn_prefill_strided.restype = ctypes.c_int
+            lib.gdn_decode_strided.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Strides), ctypes.c_int32,
+                                               ctypes.c_int32, P, P, P, P, P, P, P, P, P, P, P, f32, P, P]
+            lib.gdn_decode_strided.restype = ctypes.c_int
             lib.gdn_check_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
             lib.gdn_check_device_status.restype = ctypes.c_int
             _lib = lib
@@ -105,6 +120,43 @@ def _ptr(t: Optional[torch.Tensor], dtype, name: str, device) -> Optional[int]:
     return t.data_ptr()
 
 
+def _in_ptr(t: Optional[torch.Tensor], name: str, device) -> Optional[int]:
+    """Pointer of a token input that may be a strided view (innermost
+    dimension contiguous): checked by the library against its strides."""
+    if t is None:
+        return None
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name}: expected torch.bfloat16, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name}: expected device {device}, got {t.device}")
+    if t.stride(-1) != 1:
+        raise ValueError(f"{name}: the innermost dimension must be contiguous")
+    return t.data_ptr()
+
+
+def _token_strides(t: Optional[torch.Tensor], lead: int, name: str):
+    """(token, head) element strides of a [tokens..., heads(, 128)] view whose
+    `lead` leading dimensions flatten into the token index."""
+    if t is None:
+        return (0, 0)
+    st, sh = t.stride(lead - 1), t.stride(lead)
+    for d in range(lead - 1):   # the leading dimensions must flatten evenly
+        if t.stride(d) != t.stride(d + 1) * t.shape[d + 1]:
+            raise ValueError(f"{name}: the token dimensions do not flatten into one stride")
+    return (st, sh)
+
+
+def _strides(tensors: dict, lead: int):
+    """None when every token input is dense, else the Strides structure."""
+    if all(t is None or t.is_contiguous() for t in tensors.values()):
+        return None
+    s = Strides()
+    for n in ("q", "k", "v", "z", "a", "b"):
+        tok, head = _token_strides(tensors.get(n), lead, n)
+        setattr(s, n, Stride(tok, head))
+    return s
+
+
 def _stream_handle(stream: Optional[torch.cuda.Stream], device) -> int:
     s = stream if stream is not None else torch.cuda.current_stream(device)
     return s.cuda_stream
@@ -122,8 +174,9 @@ def prefill(q, k, v, a, b, A_log, dt_bias, cu_seqlens, init_state=None, z=None, 
             eps: float = 1e-6, out=None, final_state=None, workspace=None, stream=None):
     """Chunked GDN prefill through ``gdn_prefill``.  Returns (out, final_state).
 
-    q, k [T, Hk, 128] bf16; v [T, Hv, 128] bf16; a, b [T, Hv] bf16; A_log,
-    dt_bias [Hv] fp32; cu_seqlens [N+1] int32 (device); init_state
+    q, k [T, Hk, 128] bf16; v [T, Hv, 128] bf16; a, b [T, Hv] bf16 (dense,
+    or views with a contiguous innermost dimension, e.g. slices of one packed
+    projection output, passed as strides); A_log, dt_bias [Hv] fp32; cu_seqlens [N+1] int32 (device); init_state
     [N, Hv, 128, 128] fp32 or None; z [T, Hv, 128] bf16 and norm_w [128] bf16
     for the gated-RMSNorm epilogue.  ``final_state`` may be ``init_state``.
     """
@@ -139,14 +192,17 @@ def prefill(q, k, v, a, b, A_log, dt_bias, cu_seqlens, init_state=None, z=None, 
         workspace = alloc_workspace(N, T, hk, hv, dev)
     bf, f32 = torch.bfloat16, torch.float32
     shape = make_shape(N, T, hk, hv)
-    code = load().gdn_prefill(
-        ctypes.byref(shape), _ptr(q, bf, "q", dev), _ptr(k, bf, "k", dev), _ptr(v, bf, "v", dev),
-        _ptr(a, bf, "a", dev), _ptr(b, bf, "b", dev), _ptr(A_log, f32, "A_log", dev),
-        _ptr(dt_bias, f32, "dt_bias", dev), _ptr(init_state, f32, "init_state", dev),
-        _ptr(cu_seqlens, torch.int32, "cu_seqlens", dev), _ptr(z, bf, "z", dev),
-        _ptr(norm_w, bf, "norm_w", dev), float(eps), _ptr(out, bf, "out", dev),
-        _ptr(final_state, f32, "final_state", dev), _ptr(workspace, torch.uint8, "workspace", dev),
-        int(workspace.numel()), _stream_handle(stream, dev))
+    strides = _strides(dict(q=q, k=k, v=v, z=z, a=a, b=b), 1)
+    ins = [_in_ptr(t, n, dev) for t, n in ((q, "q"), (k, "k"), (v, "v"), (a, "a"), (b, "b"))]
+    rest = (_ptr(A_log, f32, "A_log", dev), _ptr(dt_bias, f32, "dt_bias", dev),
+            _ptr(init_state, f32, "init_state", dev), _ptr(cu_seqlens, torch.int32, "cu_seqlens", dev),
+            _in_ptr(z, "z", dev), _ptr(norm_w, bf, "norm_w", dev), float(eps), _ptr(out, bf, "out", dev),
+            _ptr(final_state, f32, "final_state", dev), _ptr(workspace, torch.uint8, "workspace", dev),
+            int(workspace.numel()), _stream_handle(stream, dev))
+    if strides is None:
+        code = load().gdn_prefill(ctypes.byref(shape), *ins, *rest)
+    else:
+        code = load().gdn_prefill_strided(ctypes.byref(shape), ctypes.byref(strides), *ins, *rest)
     _check(code)
     return out, final_state
 
@@ -216,12 +272,17 @@ def decode_slots(q, k, v, a, b, A_log, dt_bias, state_pool, state_idx=None, z=No
         out = torch.empty(B, T, hv, 128, dtype=torch.bfloat16, device=dev)
     bf, f32 = torch.bfloat16, torch.float32
     shape = make_shape(B, B * T, hk, hv)
-    code = load().gdn_decode_slots(
-        ctypes.byref(shape), int(T), int(state_pool.shape[0]), _ptr(q, bf, "q", dev), _ptr(k, bf, "k", dev),
-        _ptr(v, bf, "v", dev), _ptr(a, bf, "a", dev), _ptr(b, bf, "b", dev), _ptr(A_log, f32, "A_log", dev),
-        _ptr(dt_bias, f32, "dt_bias", dev), _ptr(state_pool, f32, "state_pool", dev),
-        _ptr(state_idx, torch.int32, "state_idx", dev), _ptr(z, bf, "z", dev), _ptr(norm_w, bf, "norm_w", dev),
-        float(eps), _ptr(out, bf, "out", dev), _stream_handle(stream, dev))
+    strides = _strides(dict(q=q, k=k, v=v, z=z, a=a, b=b), 2)
+    ins = [_in_ptr(t, n, dev) for t, n in ((q, "q"), (k, "k"), (v, "v"), (a, "a"), (b, "b"))]
+    rest = (_ptr(A_log, f32, "A_log", dev), _ptr(dt_bias, f32, "dt_bias", dev),
+            _ptr(state_pool, f32, "state_pool", dev), _ptr(state_idx, torch.int32, "state_idx", dev),
+            _in_ptr(z, "z", dev), _ptr(norm_w, bf, "norm_w", dev), float(eps), _ptr(out, bf, "out", dev),
+            _stream_handle(stream, dev))
+    if strides is None:
+        code = load().gdn_decode_slots(ctypes.byref(shape), int(T), int(state_pool.shape[0]), *ins, *rest)
+    else:
+        code = load().gdn_decode_strided(ctypes.byref(shape), ctypes.byref(strides), int(T),
+                                         int(state_pool.shape[0]), *ins, *rest)
     _check(code)
     return out
 

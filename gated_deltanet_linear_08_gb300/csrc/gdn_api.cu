@@ -56,6 +56,37 @@ gdn_status_t check_shape(const gdn_shape_t *s)
     return GDN_OK;
 }
 
+// The caller's strides, or the dense layouts when none are given; false if
+// they break the rules of gdn_strides_t.
+bool resolve_strides(const gdn_strides_t *u, int hk, int hv, bool with_z, gdn::InputStrides &o)
+{
+    const int64_t k = 128;
+    o.q = {hk * k, k}; o.k = {hk * k, k}; o.v = {hv * k, k}; o.z = {hv * k, k};
+    o.a = {hv, 1}; o.b = {hv, 1};
+    if (!u)
+        return true;
+    o.q = {u->q.token, u->q.head}; o.k = {u->k.token, u->k.head}; o.v = {u->v.token, u->v.head};
+    o.a = {u->a.token, u->a.head}; o.b = {u->b.token, u->b.head};
+    if (with_z)
+        o.z = {u->z.token, u->z.head};
+    for (const gdn::Stride &x : {o.q, o.k, o.v, o.z})
+        if (x.t <= 0 || x.h < 128 || x.t % 8 || x.h % 8)
+            return false;
+    for (const gdn::Stride &x : {o.a, o.b})
+        if (x.t <= 0 || x.h <= 0)
+            return false;
+    return true;
+}
+
+// Bytes spanned by a strided bf16 input of `tokens` x `heads` rows of `row`
+// elements (0 for an absent tensor).
+size_t span(const void *p, size_t tokens, size_t heads, const gdn::Stride &x, size_t row)
+{
+    if (!p || tokens == 0)
+        return 0;
+    return ((tokens - 1) * (size_t)x.t + (heads - 1) * (size_t)x.h + row) * 2;
+}
+
 }  // namespace
 
 extern "C" {
@@ -81,11 +112,11 @@ size_t gdn_prefill_workspace_bytes(const gdn_shape_t *s)
     return gdn::prefill_workspace_bytes(s->num_seqs, s->total_tokens, s->hk, s->hv);
 }
 
-gdn_status_t gdn_prefill(const gdn_shape_t *s, const void *q, const void *k, const void *v,
-                         const void *a, const void *b, const float *A_log, const float *dt_bias,
-                         const float *init_state, const int32_t *cu_seqlens, const void *z,
-                         const void *norm_w, float eps, void *out, float *final_state,
-                         void *workspace, size_t workspace_bytes, void *stream)
+gdn_status_t gdn_prefill_strided(const gdn_shape_t *s, const gdn_strides_t *strides, const void *q,
+                                 const void *k, const void *v, const void *a, const void *b, const float *A_log,
+                                 const float *dt_bias, const float *init_state, const int32_t *cu_seqlens,
+                                 const void *z, const void *norm_w, float eps, void *out, float *final_state,
+                                 void *workspace, size_t workspace_bytes, void *stream)
 {
     gdn_status_t st = check_shape(s);
     if (st != GDN_OK)
@@ -101,12 +132,15 @@ gdn_status_t gdn_prefill(const gdn_shape_t *s, const void *q, const void *k, con
         return GDN_ERR_INVALID_ARG;
     if (!(eps >= 0.f))
         return GDN_ERR_INVALID_ARG;
-    const void *al16[] = {q, k, v, a, b, init_state, z, norm_w, out, final_state};
+    gdn::InputStrides in;
+    if (!resolve_strides(strides, s->hk, s->hv, z != nullptr, in))
+        return GDN_ERR_INVALID_ARG;
+    const void *al16[] = {q, k, v, init_state, z, norm_w, out, final_state};
     for (const void *p : al16)
         if (p && !aligned(p, 16))
             return GDN_ERR_ALIGNMENT;
-    // a, b rows are Hv bf16 wide: every row start need not be 16-byte aligned,
-    // but the tensor base must be (checked above).
+    if (!aligned(a, 2) || !aligned(b, 2))   // read one element at a time
+        return GDN_ERR_ALIGNMENT;
     const size_t need = gdn::prefill_workspace_bytes(s->num_seqs, s->total_tokens, s->hk, s->hv);
     if (need > 0 && (!workspace || workspace_bytes < need))
         return GDN_ERR_WORKSPACE;
@@ -116,9 +150,9 @@ gdn_status_t gdn_prefill(const gdn_shape_t *s, const void *q, const void *k, con
     const size_t out_b = T * hv * 128 * 2;
     const size_t st_b = N * hv * 128 * 128 * 4;
     const struct { const void *p; size_t n; } ins[] = {
-        {q, T * hk * 256}, {k, T * hk * 256}, {v, T * hv * 256}, {a, T * hv * 2},
-        {b, T * hv * 2}, {z, z ? T * hv * 256 : 0}, {init_state, init_state ? st_b : 0},
-        {cu_seqlens, (N + 1) * 4}, {workspace, need}};
+        {q, span(q, T, hk, in.q, 128)}, {k, span(k, T, hk, in.k, 128)}, {v, span(v, T, hv, in.v, 128)},
+        {a, span(a, T, hv, in.a, 1)}, {b, span(b, T, hv, in.b, 1)}, {z, span(z, T, hv, in.z, 128)},
+        {init_state, init_state ? st_b : 0}, {cu_seqlens, (N + 1) * 4}, {workspace, need}};
     for (const auto &x : ins)
         if (overlaps(out, out_b, x.p, x.n))
             return GDN_ERR_INVALID_ARG;
@@ -133,6 +167,7 @@ gdn_status_t gdn_prefill(const gdn_shape_t *s, const void *q, const void *k, con
     p.hk = s->hk;
     p.hv = s->hv;
     p.max_chunks = gdn::prefill_max_chunks(s->num_seqs, s->total_tokens);
+    p.in = in;
     p.q = q; p.k = k; p.v = v; p.a = a; p.b = b;
     p.A_log = A_log; p.dt_bias = dt_bias;
     p.init_state = init_state;
@@ -147,10 +182,21 @@ gdn_status_t gdn_prefill(const gdn_shape_t *s, const void *q, const void *k, con
     return gdn::launch_prefill(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
-gdn_status_t gdn_decode_slots(const gdn_shape_t *s, int32_t tokens, int32_t num_slots, const void *q,
-                              const void *k, const void *v, const void *a, const void *b, const float *A_log,
-                              const float *dt_bias, float *state, const int32_t *state_idx, const void *z,
-                              const void *norm_w, float eps, void *out, void *stream)
+gdn_status_t gdn_prefill(const gdn_shape_t *s, const void *q, const void *k, const void *v,
+                         const void *a, const void *b, const float *A_log, const float *dt_bias,
+                         const float *init_state, const int32_t *cu_seqlens, const void *z,
+                         const void *norm_w, float eps, void *out, float *final_state,
+                         void *workspace, size_t workspace_bytes, void *stream)
+{
+    return gdn_prefill_strided(s, nullptr, q, k, v, a, b, A_log, dt_bias, init_state, cu_seqlens, z, norm_w,
+                               eps, out, final_state, workspace, workspace_bytes, stream);
+}
+
+gdn_status_t gdn_decode_strided(const gdn_shape_t *s, const gdn_strides_t *strides, int32_t tokens,
+                                int32_t num_slots, const void *q, const void *k, const void *v, const void *a,
+                                const void *b, const float *A_log, const float *dt_bias, float *state,
+                                const int32_t *state_idx, const void *z, const void *norm_w, float eps,
+                                void *out, void *stream)
 {
     gdn_status_t st = check_shape(s);
     if (st != GDN_OK)
@@ -170,18 +216,23 @@ gdn_status_t gdn_decode_slots(const gdn_shape_t *s, int32_t tokens, int32_t num_
         return GDN_ERR_INVALID_ARG;
     if (!(eps >= 0.f))
         return GDN_ERR_INVALID_ARG;
-    const void *al16[] = {q, k, v, a, b, state, z, norm_w, out};
+    gdn::InputStrides in;
+    if (!resolve_strides(strides, s->hk, s->hv, z != nullptr, in))
+        return GDN_ERR_INVALID_ARG;
+    const void *al16[] = {q, k, v, state, z, norm_w, out};
     for (const void *p : al16)
         if (p && !aligned(p, 16))
             return GDN_ERR_ALIGNMENT;
+    if (!aligned(a, 2) || !aligned(b, 2))   // read one element at a time
+        return GDN_ERR_ALIGNMENT;
     if (state_idx && !aligned(state_idx, 4))
         return GDN_ERR_ALIGNMENT;
     const size_t hk = s->hk, hv = s->hv, BT = B * (size_t)tokens;
     const size_t out_b = BT * hv * 256;
     const struct { const void *p; size_t n; } ins[] = {
-        {q, BT * hk * 256}, {k, BT * hk * 256}, {v, BT * hv * 256}, {a, BT * hv * 2},
-        {b, BT * hv * 2}, {z, z ? BT * hv * 256 : 0}, {state, (size_t)num_slots * hv * 128 * 128 * 4},
-        {state_idx, state_idx ? B * 4 : 0}};
+        {q, span(q, BT, hk, in.q, 128)}, {k, span(k, BT, hk, in.k, 128)}, {v, span(v, BT, hv, in.v, 128)},
+        {a, span(a, BT, hv, in.a, 1)}, {b, span(b, BT, hv, in.b, 1)}, {z, span(z, BT, hv, in.z, 128)},
+        {state, (size_t)num_slots * hv * 128 * 128 * 4}, {state_idx, state_idx ? B * 4 : 0}};
     for (const auto &x : ins)
         if (overlaps(out, out_b, x.p, x.n))
             return GDN_ERR_INVALID_ARG;
@@ -193,6 +244,7 @@ gdn_status_t gdn_decode_slots(const gdn_shape_t *s, int32_t tokens, int32_t num_
     p.tokens = tokens;
     p.num_slots = num_slots;
     p.state_idx = state_idx;
+    p.in = in;
     p.q = q; p.k = k; p.v = v; p.a = a; p.b = b;
     p.A_log = A_log; p.dt_bias = dt_bias;
     p.state = state;
@@ -202,6 +254,15 @@ gdn_status_t gdn_decode_slots(const gdn_shape_t *s, int32_t tokens, int32_t num_
     if (!p.status)
         return GDN_ERR_CUDA;
     return gdn::launch_decode(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status_t gdn_decode_slots(const gdn_shape_t *s, int32_t tokens, int32_t num_slots, const void *q,
+                              const void *k, const void *v, const void *a, const void *b, const float *A_log,
+                              const float *dt_bias, float *state, const int32_t *state_idx, const void *z,
+                              const void *norm_w, float eps, void *out, void *stream)
+{
+    return gdn_decode_strided(s, nullptr, tokens, num_slots, q, k, v, a, b, A_log, dt_bias, state, state_idx, z,
+                              norm_w, eps, out, stream);
 }
 
 gdn_status_t gdn_decode(const gdn_shape_t *s, const void *q, const void *k, const void *v,

@@ -69,8 +69,9 @@ decode_kernel(DecodeArgs p)
         // 2. Per-token inputs: warp 0 normalises k, warp 1 q, warp 2 loads v,
         //    warp 3 computes the gate and beta.
         if (warp < 2) {
+            const Stride sd = warp == 0 ? p.in.k : p.in.q;
             const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(warp == 0 ? p.k : p.q)
-                                       + (tok * hk + hq) * kD + lane * 4;
+                                       + (int64_t)tok * sd.t + (int64_t)hq * sd.h + lane * 4;
             const uint2 u = *reinterpret_cast<const uint2 *>(src);
             float f[4] = {__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
                           __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u)};
@@ -84,15 +85,16 @@ decode_kernel(DecodeArgs p)
             for (int j = 0; j < 4; ++j)
                 dst[lane * 4 + j] = f[j] * r;
         } else if (warp == 2) {
-            const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(p.v) + (tok * hv + h) * kD + lane * 4;
+            const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(p.v)
+                                       + (int64_t)tok * p.in.v.t + (int64_t)h * p.in.v.h + lane * 4;
             const uint2 u = *reinterpret_cast<const uint2 *>(src);
             s_v[lane * 4 + 0] = __uint_as_float(u.x << 16);
             s_v[lane * 4 + 1] = __uint_as_float(u.x & 0xFFFF0000u);
             s_v[lane * 4 + 2] = __uint_as_float(u.y << 16);
             s_v[lane * 4 + 3] = __uint_as_float(u.y & 0xFFFF0000u);
         } else if (warp == 3 && lane == 0) {
-            const float av = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.a)[tok * hv + h]);
-            const float bv = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.b)[tok * hv + h]);
+            const float av = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.a)[(int64_t)tok * p.in.a.t + (int64_t)h * p.in.a.h]);
+            const float bv = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.b)[(int64_t)tok * p.in.b.t + (int64_t)h * p.in.b.h]);
             s_scal[0] = expf(gate_f(av, p.A_log[h], p.dt_bias[h]));
             s_scal[1] = sigmoid_f(bv);
         }
@@ -153,7 +155,8 @@ decode_kernel(DecodeArgs p)
         if (tid < kD) {
             if (kNorm) {
                 const float ms = (s_red[0] + s_red[1] + s_red[2] + s_red[3]) * (1.f / kD);
-                const float zz = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.z)[(tok * hv + h) * kD + tid]);
+                const float zz = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.z)[(int64_t)tok * p.in.z.t
+                                                                                   + (int64_t)h * p.in.z.h + tid]);
                 const float ww = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.norm_w)[tid]);
                 o = o * rsqrtf(ms + p.eps) * ww * (zz * sigmoid_f(zz));
             }

@@ -291,10 +291,10 @@ cudaError_t launch_prefill_out(const PrefillArgs &p, cudaStream_t stream)
         configured = true;
     }
     CUtensorMap tz, to;
-    if (!encode_tile_map(&to, p.out, p.hv, p.total_tokens))
+    if (!encode_tile_map(&to, p.out, p.hv, p.total_tokens, (int64_t)p.hv * kD, kD))
         return cudaErrorInvalidValue;
     if (p.z) {
-        if (!encode_tile_map(&tz, p.z, p.hv, p.total_tokens))
+        if (!encode_tile_map(&tz, p.z, p.hv, p.total_tokens, p.in.z.t, p.in.z.h))
             return cudaErrorInvalidValue;
     } else {
         tz = to;   // unused without the epilogue

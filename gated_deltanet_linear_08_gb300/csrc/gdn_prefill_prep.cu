@@ -250,9 +250,10 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
     if (tid < 64) {
         float gv = 0.f, bv = 0.f;
         if (tid < L) {
-            const size_t idx = (size_t)(tok0 + tid) * hv + h;
-            gv = gate_f(bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.a)[idx]), p.A_log[h], p.dt_bias[h]);
-            bv = sigmoid_f(bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.b)[idx]));
+            const int64_t tok = tok0 + tid;
+            gv = gate_f(bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.a)[tok * p.in.a.t + h * p.in.a.h]),
+                        p.A_log[h], p.dt_bias[h]);
+            bv = sigmoid_f(bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.b)[tok * p.in.b.t + h * p.in.b.h]));
         }
         float c = gv;
 #pragma unroll
@@ -683,15 +684,14 @@ EncodeTiledFn encode_fn()
 
 }  // namespace
 
-// Tensor map over a bf16 [T][heads][128] tensor: boxes of 64 tokens x 64
-// dims of one head, 128-byte swizzled in shared memory, zero fill past T.
-bool encode_tile_map(CUtensorMap *map, const void *base, int heads, int tokens)
+// Tensor map over token x head rows of 128 bf16 (see kernels.h).
+bool encode_tile_map(CUtensorMap *map, const void *base, int heads, int tokens, int64_t st, int64_t sh)
 {
     const EncodeTiledFn fn = encode_fn();
-    if (!fn)
+    if (!fn || st <= 0 || sh <= 0)
         return false;
     const cuuint64_t dims[3] = {128, (cuuint64_t)heads, (cuuint64_t)tokens};
-    const cuuint64_t strides[2] = {256, (cuuint64_t)heads * 256};
+    const cuuint64_t strides[2] = {(cuuint64_t)sh * 2, (cuuint64_t)st * 2};
     const cuuint32_t box[3] = {64, 1, 64};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
@@ -710,8 +710,9 @@ cudaError_t launch_prefill_prep(const PrefillArgs &p, cudaStream_t stream)
         configured = true;
     }
     CUtensorMap tq, tk, tv;
-    if (!encode_tile_map(&tq, p.q, p.hk, p.total_tokens) || !encode_tile_map(&tk, p.k, p.hk, p.total_tokens)
-        || !encode_tile_map(&tv, p.v, p.hv, p.total_tokens))
+    if (!encode_tile_map(&tq, p.q, p.hk, p.total_tokens, p.in.q.t, p.in.q.h)
+        || !encode_tile_map(&tk, p.k, p.hk, p.total_tokens, p.in.k.t, p.in.k.h)
+        || !encode_tile_map(&tv, p.v, p.hv, p.total_tokens, p.in.v.t, p.in.v.h))
         return cudaErrorInvalidValue;
     dim3 grid(p.max_chunks, p.hv);
     prep_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p, tq, tk, tv);

@@ -9,11 +9,22 @@
 
 namespace gdn {
 
+// Element strides of one token input: between consecutive tokens and
+// between consecutive heads (rows of 128 elements for q, k, v, z; one element
+// for a, b).
+struct Stride {
+    int64_t t, h;
+};
+struct InputStrides {
+    Stride q, k, v, z, a, b;
+};
+
 struct DecodeArgs {
     int batch, hk, hv;
     int tokens;                    // consecutive tokens per sequence (1..8)
     int num_slots;                 // slots in the state pool
     const int32_t *state_idx;      // slot per sequence, or null for slot n
+    InputStrides in;
     const void *q, *k, *v, *a, *b;
     const float *A_log, *dt_bias;
     float *state;                  // state pool [num_slots, hv, 128, 128]
@@ -26,6 +37,7 @@ struct DecodeArgs {
 struct PrefillArgs {
     int num_seqs, total_tokens, hk, hv;
     int max_chunks;                // upper bound on chunks: ceil(T/64) + N
+    InputStrides in;
     const void *q, *k, *v, *a, *b;
     const float *A_log, *dt_bias;
     const float *init_state;
@@ -75,11 +87,12 @@ inline size_t prefill_workspace_bytes(int num_seqs, int total_tokens, int hk, in
     return c * (size_t)hv * kPerVHead;
 }
 
-// Tensor map over a bf16 [tokens][heads][128] tensor: boxes of 64 tokens x 64
-// dims of one head, 128-byte swizzled in shared memory, zero fill past the
-// last token.  Host only; false if the driver's encoder is unavailable or
-// rejects the tensor.
-bool encode_tile_map(CUtensorMap *map, const void *base, int heads, int tokens);
+// Tensor map over a bf16 tensor of `tokens` x `heads` rows of 128 elements,
+// `st` elements between tokens and `sh` between heads (multiples of 8): boxes
+// of 64 tokens x 64 elements of one head, 128-byte swizzled in shared memory,
+// zero fill past the last token.  Host only; false if the driver's encoder is
+// unavailable or rejects the tensor.
+bool encode_tile_map(CUtensorMap *map, const void *base, int heads, int tokens, int64_t st, int64_t sh);
 
 cudaError_t launch_decode(const DecodeArgs &args, cudaStream_t stream);
 // The chunked prefill runs three kernels in stream order: prep (chunk-parallel

@@ -26,7 +26,8 @@
  *     gdn_prefill / gdn_decode.
  *   - Layouts are row-major, innermost index last, densely packed.
  *   - bf16 tensors and fp32 state/workspace pointers must be 16-byte aligned
- *     (GDN_ERR_ALIGNMENT otherwise); the workspace must be 1024-byte aligned.
+ *     (GDN_ERR_ALIGNMENT otherwise), except a and b (2-byte, read element by
+ *     element); the workspace must be 1024-byte aligned.
  *   - Only Dk = Dv = 128, Hq == Hk and Hv % Hk == 0 are supported; anything
  *     else returns GDN_ERR_UNSUPPORTED before any launch.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
@@ -183,6 +184,53 @@ gdn_status_t gdn_decode_slots(const gdn_shape_t *shape, int32_t tokens, int32_t 
                               float *state_pool, const int32_t *state_idx,
                               const void *z, const void *norm_w, float eps,
                               void *out, void *stream);
+
+/*
+ * Strided token inputs, for reading q, k, v, z, a and b in place from one
+ * packed projection output (SGLang page "[Perf] Pack the Qwen3.5 GDN input
+ * projection on CUDA": a single GEMM on the packed in_proj_qkvz and
+ * in_proj_ba weights writes every token's q, k, v, z, b and a side by side;
+ * 12,352 elements per token for the Qwen3.5-4B geometry).  For each tensor,
+ * `token` is the distance in elements between consecutive tokens and `head`
+ * between consecutive heads; a head of q, k, v or z is 128 contiguous
+ * elements, a head of a or b one element.  The dense layouts of gdn_prefill
+ * and gdn_decode are {Hk*128, 128} for q and k, {Hv*128, 128} for v and z and
+ * {Hv, 1} for a and b.
+ * Requirements (else GDN_ERR_INVALID_ARG): every stride positive; for q, k,
+ * v and z both strides multiples of 8 elements (16 bytes) and head >= 128.
+ * z's strides are ignored when z is NULL.
+ */
+typedef struct {
+    int64_t token;
+    int64_t head;
+} gdn_stride_t;
+
+typedef struct {
+    gdn_stride_t q, k, v, z, a, b;
+} gdn_strides_t;
+
+/* gdn_prefill with strided token inputs (strides NULL: the dense layouts).
+ * `out` is dense [T_tot, Hv, 128] and must not overlap the span of any input. */
+gdn_status_t gdn_prefill_strided(const gdn_shape_t *shape, const gdn_strides_t *strides,
+                                 const void *q, const void *k, const void *v,
+                                 const void *a, const void *b,
+                                 const float *A_log, const float *dt_bias,
+                                 const float *init_state, const int32_t *cu_seqlens,
+                                 const void *z, const void *norm_w, float eps,
+                                 void *out, float *final_state,
+                                 void *workspace, size_t workspace_bytes,
+                                 void *stream);
+
+/* gdn_decode_slots with strided token inputs (strides NULL: the dense
+ * layouts); the token index is n * tokens + t.  `out` is dense. */
+gdn_status_t gdn_decode_strided(const gdn_shape_t *shape, const gdn_strides_t *strides,
+                                int32_t tokens, int32_t num_slots,
+                                const void *q, const void *k, const void *v,
+                                const void *a, const void *b,
+                                const float *A_log, const float *dt_bias,
+                                float *state_pool, const int32_t *state_idx,
+                                const void *z, const void *norm_w, float eps,
+                                void *out, void *stream);
 
 /* Reads and clears the device status word that kernels set when a bounded
  * wait runs out.  Synchronises the device: not for the hot path.  Returns

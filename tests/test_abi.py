@@ -131,6 +131,41 @@ def test_decode_slots_rejects_bad_arguments(lib):
     assert dec(B.make_shape(0, 0, 16, 32)) == 0                   # empty batch: no-op
 
 
+def test_strided_entry_points_reject_bad_strides(lib):
+    # host-side validation only: every call here fails before any launch
+    def strides(**over):
+        base = dict(q=(16 * 128, 128), k=(16 * 128, 128), v=(32 * 128, 128), z=(32 * 128, 128),
+                    a=(32, 1), b=(32, 1))
+        base.update(over)
+        return B.Strides(*(B.Stride(*base[n]) for n in ("q", "k", "v", "z", "a", "b")))
+
+    def pre(st):
+        return lib.gdn_prefill_strided(ctypes.byref(B.make_shape(1, 64, 16, 32)), ctypes.byref(st), FAKE,
+                                       FAKE + 0x10000000, FAKE + 0x20000000, FAKE + 0x30000000,
+                                       FAKE + 0x40000000, FAKE + 0x50000000, FAKE + 0x60000000, None,
+                                       FAKE + 0x80000000, None, None, 1e-6, FAKE + 0x90000000,
+                                       FAKE + 0xA0000000, FAKE + 0xB0000000, 1 << 30, None)
+
+    def dec(st):
+        return lib.gdn_decode_strided(ctypes.byref(B.make_shape(4, 8, 16, 32)), ctypes.byref(st), 2, 8, FAKE,
+                                      FAKE + 0x10000000, FAKE + 0x20000000, FAKE + 0x30000000,
+                                      FAKE + 0x40000000, FAKE + 0x50000000, FAKE + 0x60000000,
+                                      FAKE + 0x70000000, None, None, None, 1e-6, FAKE + 0x90000000, None)
+    for call in (pre, dec):
+        assert call(strides(q=(16 * 128 + 4, 128))) == 1   # not a multiple of 8 elements
+        assert call(strides(k=(16 * 128, 64))) == 1        # heads closer than a 128-element row
+        assert call(strides(v=(0, 128))) == 1              # zero token stride
+        assert call(strides(a=(32, 0))) == 1
+    # a packed projection row: q | k | v | z | b | a, 12,352 elements per token
+    W = 2 * 16 * 128 + 2 * 32 * 128 + 2 * 32
+    packed = strides(q=(W, 128), k=(W, 128), v=(W, 128), z=(W, 128), a=(W, 1), b=(W, 1))
+    # out must not lie inside the span of the packed inputs
+    assert lib.gdn_prefill_strided(ctypes.byref(B.make_shape(1, 64, 16, 32)), ctypes.byref(packed), FAKE,
+                                   FAKE + 4096, FAKE + 8192, FAKE + 24640, FAKE + 24576, FAKE + 0x50000000,
+                                   FAKE + 0x60000000, None, FAKE + 0x80000000, None, None, 1e-6,
+                                   FAKE + 64 * W, FAKE + 0xA0000000, FAKE + 0xB0000000, 1 << 30, None) == 1
+
+
 def test_missing_library_fails_loudly(tmp_path):
     saved = B._lib
     try:

@@ -1,0 +1,72 @@
+"""GPU: the token inputs read in place from one packed projection output (SGLang
+page "[Perf] Pack the Qwen3.5 GDN input projection on CUDA": a single GEMM on
+the packed in_proj_qkvz and in_proj_ba weights writes each token's q, k, v,
+z, b and a side by side).  The row order used here, q | k | v | z | b | a
+(in_proj_qkvz rows, then in_proj_ba rows), is a reading: the page gives the
+packed width but not the order, and the strided entry points accept any
+order of head-contiguous blocks.  Results must equal the dense call bit for
+bit: the same values reach the same arithmetic.
+"""
+import pytest
+import torch
+
+from gated_deltanet_linear_08_gb300.inputs import (DecodeSlotsCase, PrefillCase, make_decode_slots_inputs,
+                                                   make_prefill_inputs)
+from parity_util import to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _pack(q, k, v, z, b, a):
+    """One [tokens..., W] buffer holding q | k | v | z | b | a per token, and
+    strided views of it shaped like the dense tensors."""
+    lead = q.shape[:-2]
+    parts = [q.flatten(-2), k.flatten(-2), v.flatten(-2), z.flatten(-2), b, a]
+    W = sum(p.shape[-1] for p in parts)
+    pad = (-W) % 8   # keep every block 16-byte aligned
+    buf = torch.zeros(*lead, W + pad, dtype=torch.bfloat16, device=q.device)
+    views, off = [], 0
+    for p in parts:
+        n = p.shape[-1]
+        buf[..., off:off + n] = p
+        views.append(buf[..., off:off + n])
+        off += n
+    qv = views[0].unflatten(-1, q.shape[-2:])
+    kv = views[1].unflatten(-1, k.shape[-2:])
+    vv = views[2].unflatten(-1, v.shape[-2:])
+    zv = views[3].unflatten(-1, z.shape[-2:])
+    return buf, qv, kv, vv, zv, views[4], views[5]
+
+
+def test_prefill_reads_inputs_from_a_packed_projection():
+    import gated_deltanet_linear_08_gb300 as gdn
+    x = make_prefill_inputs(PrefillCase("packed", seqlens=[200, 64, 1, 90], hk=2, hv=4, init_state=True,
+                                        gated_norm=True, seed=31))
+    d = to_dev(x)
+    ref_out, ref_fin = gdn.prefill(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"],
+                                   d["cu_seqlens"], init_state=d["init_state"], z=d["z"], norm_w=d["norm_w"],
+                                   eps=x["eps"])
+    buf, q, k, v, z, b, a = _pack(d["q"], d["k"], d["v"], d["z"], d["b"], d["a"])
+    assert not q.is_contiguous() and q.stride(0) == buf.shape[-1]
+    out, fin = gdn.prefill(q, k, v, a, b, d["A_log"], d["dt_bias"], d["cu_seqlens"], init_state=d["init_state"],
+                           z=z, norm_w=d["norm_w"], eps=x["eps"])
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_out) and torch.equal(fin, ref_fin)
+    assert gdn.check_device_status() == 0
+
+
+def test_decode_reads_inputs_from_a_packed_projection():
+    import gated_deltanet_linear_08_gb300 as gdn
+    x = make_decode_slots_inputs(DecodeSlotsCase("packed_dec", batch=10, tokens=3, slots=16, skipped=1,
+                                                 hk=2, hv=4, gated_norm=True, seed=32))
+    dev = "cuda"
+    t = {n: x[n].to(dev) for n in ("q", "k", "v", "a", "b", "z")}
+    A_log, dt, idx, w = x["A_log"].to(dev), x["dt_bias"].to(dev), x["state_idx"].to(dev), x["norm_w"].to(dev)
+    pool_ref, pool = x["pool"].to(dev), x["pool"].to(dev)
+    ref = gdn.decode_slots(t["q"], t["k"], t["v"], t["a"], t["b"], A_log, dt, pool_ref, state_idx=idx,
+                           z=t["z"], norm_w=w)
+    buf, q, k, v, z, b, a = _pack(t["q"], t["k"], t["v"], t["z"], t["b"], t["a"])
+    got = gdn.decode_slots(q, k, v, a, b, A_log, dt, pool, state_idx=idx, z=z, norm_w=w)
+    torch.cuda.synchronize()
+    assert torch.equal(got, ref) and torch.equal(pool, pool_ref)
+    assert gdn.check_device_status() == 0
