@@ -15,6 +15,10 @@ Parity status of each function (what pins it, see tests/test_oracle.py):
   gated_rmsnorm        unit RMS after dividing out w*silu(z); hand-computed
                        fixture.
   prefill / decode     compositions of the above.
+  causal_conv_silu /   impulse weights reduce it to shifted inputs, numpy's
+  conv_inputs          np.convolve per channel, split-sequence state carry;
+                       the conv itself is a reading (nothing on the pages
+                       defines it), so its parity is unpinned by the pages.
 The grouped-head mapping (v head h reads k head h // (Hv/Hk)), the L2-norm
 epsilon 1e-6 and the per-head gated-norm grouping are readings of the pages,
 not facts they print: parity of those choices is unpinned by the pages.
@@ -207,3 +211,67 @@ def decode_step(q, k, v, a, b, A_log, dt_bias, state, z=None, norm_w=None,
     if rc != 0:
         raise ValueError("oracle decode_step: bad arguments")
     return out
+
+
+# ---------------------------------------------------------------------------
+# Causal conv1d + SiLU ahead of the core.  The JevAny page ("Add opt-in fused
+# Qwen3.5 inference kernels", Measurements) lists causal-conv1d among the
+# path's dependencies but does not define it; the definition below is a
+# reading (plain numpy, fp64):
+#   * channels: q | k | v of a token, Hk*128 + Hk*128 + Hv*128 of them;
+#   * per channel c a causal window of width K (1..4) with weights w[c, 0..K-1]:
+#         y[t, c] = silu( sum_j w[c, j] * x[t - (K-1) + j, c] )
+#     where positions before the sequence start come from the carried state
+#     (the K-1 raw inputs that preceded it, oldest first) or are zero;
+#   * y is rounded to bf16 (round to nearest even), as a separate conv pass
+#     would write it, and the core then runs on those values;
+#   * the new state is the sequence's last K-1 raw inputs (state rows first
+#     when the sequence is shorter than K-1).
+# ---------------------------------------------------------------------------
+def round_bf16(x):
+    """Round fp64 values to the nearest bf16 value (ties to even); finite
+    inputs in the normal range, as on the path."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)                    # x = m * 2^e, 0.5 <= |m| < 1
+    return np.ldexp(np.rint(m * 256.0) / 256.0, e)   # 8 significant bits
+
+
+def silu(x):
+    x = np.asarray(x, dtype=np.float64)
+    return x / (1.0 + np.exp(-x))
+
+
+def causal_conv_silu(x, w, state=None):
+    """One sequence: x [T, C] raw inputs, w [C, K], state [K-1, C] or None.
+    Returns (y [T, C] bf16-rounded, new state [K-1, C])."""
+    x = np.asarray(x, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    T, C = x.shape
+    K = w.shape[1]
+    prev = np.zeros((K - 1, C)) if state is None else np.asarray(state, dtype=np.float64)
+    xe = np.concatenate([prev, x], axis=0)          # [K-1+T, C]
+    acc = np.zeros((T, C))
+    for j in range(K):
+        acc += w[:, j][None, :] * xe[j:j + T]
+    return round_bf16(silu(acc)), xe[T:T + K - 1] if K > 1 else np.zeros((0, C))
+
+
+def conv_inputs(cu_seqlens, q, k, v, w, state=None):
+    """The conv over packed sequences: q, k [T, Hk, D], v [T, Hv, D], w
+    [Hk*D + Hk*D + Hv*D, K], state [N, K-1, C] or None.  Returns the post-conv
+    q, k, v (bf16-rounded fp64) and the new states [N, K-1, C]."""
+    cu = np.asarray(cu_seqlens)
+    T, hk, d = q.shape
+    hv = v.shape[1]
+    x = np.concatenate([np.asarray(q, np.float64).reshape(T, -1), np.asarray(k, np.float64).reshape(T, -1),
+                        np.asarray(v, np.float64).reshape(T, -1)], axis=1)
+    C, K = x.shape[1], np.asarray(w).shape[1]
+    y = np.zeros_like(x)
+    new = np.zeros((len(cu) - 1, K - 1, C))
+    for n in range(len(cu) - 1):
+        s, e = cu[n], cu[n + 1]
+        y[s:e], new[n] = causal_conv_silu(x[s:e], w, None if state is None else state[n])
+    qc = y[:, :hk * d].reshape(T, hk, d)
+    kc = y[:, hk * d:2 * hk * d].reshape(T, hk, d)
+    vc = y[:, 2 * hk * d:].reshape(T, hv, d)
+    return qc, kc, vc, new

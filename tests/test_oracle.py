@@ -345,3 +345,61 @@ def test_multi_token_decode_equals_recurrence_over_the_draft():
     o2, f2 = oracle.core(np.array([0, T], np.int32), g, beta, qn, kn, v, S0)
     np.testing.assert_allclose(np.stack(outs), o2, rtol=0, atol=1e-12)
     np.testing.assert_allclose(S, f2, rtol=0, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# causal conv1d + SiLU ahead of the core (a reading: the pages list the
+# dependency without defining it)
+# --------------------------------------------------------------------------
+def test_round_bf16_matches_torch_for_fp32_values():
+    import torch
+    x = (RNG.standard_normal(4000) * np.exp(RNG.uniform(-8, 8, 4000))).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(oracle.round_bf16(x.astype(np.float64)), ref)
+
+
+def test_conv_impulse_weights_give_silu_and_shifts():
+    T, C, K = 9, 6, 4
+    x = oracle.round_bf16(RNG.standard_normal((T, C)))
+    st = oracle.round_bf16(RNG.standard_normal((K - 1, C)))
+    w = np.zeros((C, K)); w[:, K - 1] = 1.0          # current token only
+    y, new = oracle.causal_conv_silu(x, w, st)
+    assert np.array_equal(y, oracle.round_bf16(x / (1 + np.exp(-x))))
+    assert np.array_equal(new, x[T - (K - 1):])
+    w = np.zeros((C, K)); w[:, 0] = 1.0              # the token K-1 steps back
+    y, _ = oracle.causal_conv_silu(x, w, st)
+    xe = np.concatenate([st, x])
+    assert np.array_equal(y, oracle.round_bf16(xe[:T] / (1 + np.exp(-xe[:T]))))
+    y0, _ = oracle.causal_conv_silu(x, w, None)      # no state: zeros before the start
+    assert np.array_equal(y0[:K - 1], np.zeros((K - 1, C)))
+
+
+def test_conv_matches_numpy_convolve_per_channel():
+    T, C, K = 37, 5, 4
+    x = RNG.standard_normal((T, C)); w = RNG.standard_normal((C, K)); st = RNG.standard_normal((K - 1, C))
+    y, _ = oracle.causal_conv_silu(x, w, st)
+    xe = np.concatenate([st, x])
+    for c in range(C):
+        acc = np.convolve(xe[:, c], w[c, ::-1], mode="valid")   # a correlation with w
+        np.testing.assert_allclose(y[:, c], oracle.round_bf16(acc / (1 + np.exp(-acc))), rtol=0, atol=0)
+
+
+def test_conv_split_sequence_carries_the_state():
+    T, C = 23, 7
+    for K in (2, 3, 4):
+        x = RNG.standard_normal((T, C)); w = RNG.standard_normal((C, K)); st = RNG.standard_normal((K - 1, C))
+        y, new = oracle.causal_conv_silu(x, w, st)
+        for cut in (1, 2, 5, 22):
+            y1, s1 = oracle.causal_conv_silu(x[:cut], w, st)
+            y2, s2 = oracle.causal_conv_silu(x[cut:], w, s1)
+            assert np.array_equal(np.concatenate([y1, y2]), y) and np.array_equal(s2, new)
+
+
+def test_conv_inputs_channel_order_is_q_k_v():
+    T, hk, hv, d = 5, 2, 4, 128
+    q = RNG.standard_normal((T, hk, d)); k = RNG.standard_normal((T, hk, d)); v = RNG.standard_normal((T, hv, d))
+    C = 2 * hk * d + hv * d
+    w = np.zeros((C, 4)); w[2 * hk * d:, 3] = 1.0      # only the v channels pass the current token
+    qc, kc, vc, _ = oracle.conv_inputs(np.array([0, T]), q, k, v, w)
+    assert np.all(qc == 0) and np.all(kc == 0)
+    assert np.array_equal(vc, oracle.round_bf16(v / (1 + np.exp(-v))))
