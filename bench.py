@@ -34,14 +34,15 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from gated_deltanet_linear_08_gb300.inputs import (CASE_DECODE, CASE_T2048, DecodeCase,  # noqa: E402
-                                                   DecodeSlotsCase, PrefillCase, make_decode_inputs,
-                                                   make_decode_slots_inputs, make_prefill_inputs)
+                                                   DecodeSlotsCase, PrefillCase, conv_channels, make_conv_inputs,
+                                                   make_decode_inputs, make_decode_slots_inputs,
+                                                   make_prefill_inputs)
 
 METRIC = "GDN prefill tokens/s & decode GB/s at Hv=32,D=128; % of tensor/HBM roofline"
 PREFILL_FLOP_PER_TOKEN_HEAD = 10 * 64 * 128 + 6 * 128 * 128   # 180,224 (C=64 chunked count)
 N_ROTATE = 8
 KERNEL_SOURCES = ["gdn_api.cu", "gdn_decode.cu", "gdn_prefill_prep.cu", "gdn_prefill_scan.cu",
-                  "gdn_prefill_out.cu", "common.cuh", "tc05.cuh", "kernels.h"]
+                  "gdn_prefill_out.cu", "common.cuh", "conv.cuh", "tc05.cuh", "kernels.h"]
 
 
 def load_peaks():
@@ -362,6 +363,57 @@ def decode_slots_region(gdn, dev, stream, calls: int = 50, warmup: int = 5):
     return start.elapsed_time(end) / calls
 
 
+def time_calls(call, calls: int, warmup: int, stream) -> float:
+    """Device time per call of call(i) on `stream`, by CUDA events."""
+    for i in range(warmup):
+        call(i)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(calls):
+        call(i)
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / calls
+
+
+CONV_WIDTH = 4
+
+
+def conv_prefill_region(gdn, pre, stream, calls: int = 30, warmup: int = 3):
+    """The T = 2048 prefill with the width-4 causal conv + SiLU fused ahead of
+    the core (weights [8192, 4], a carried conv state in and out)."""
+    x, shared, sets = pre
+    C = conv_channels(16, x["hv"])
+    cv = make_conv_inputs(C, CONV_WIDTH, 1, seed=1)
+    w = cv["weight"].to(sets[0]["q"].device)
+    states = [cv["state"].to(w.device) for _ in sets]
+    outs = [torch.empty_like(st) for st in states]
+
+    def call(i):
+        s = sets[i % len(sets)]
+        gdn.prefill(s["q"], s["k"], s["v"], s["a"], s["b"], shared["A_log"], shared["dt_bias"],
+                    shared["cu_seqlens"], init_state=None, z=s["z"], norm_w=shared["norm_w"], eps=x["eps"],
+                    out=s["out"], final_state=s["fin"], workspace=s["ws"], stream=stream, conv_weight=w,
+                    conv_state=states[i % len(sets)], conv_state_out=outs[i % len(sets)])
+    return time_calls(call, calls, warmup, stream)
+
+
+def conv_decode_region(gdn, dec, stream, calls: int = 50, warmup: int = 5):
+    """Batch-256 decode with the width-4 conv: the conv-state pool [256, 3,
+    8192] rolled in place by the follow-up kernel."""
+    B, hv = dec["q"].shape[0], dec["v"].shape[1]
+    cv = make_conv_inputs(conv_channels(16, hv), CONV_WIDTH, B, seed=2)
+    w, cpool = cv["weight"].to(dec["q"].device), cv["state"].to(dec["q"].device)
+    tok = {n: dec[n].unsqueeze(1) for n in ("q", "k", "v", "a", "b")}
+    out = dec["out"].unsqueeze(1)
+
+    def call(i):
+        gdn.decode_slots(tok["q"], tok["k"], tok["v"], tok["a"], tok["b"], dec["A_log"], dec["dt_bias"],
+                         dec["state"], out=out, stream=stream, conv_weight=w, conv_state=cpool)
+    return time_calls(call, calls, warmup, stream)
+
+
 def cpu_baseline():
     pre = _oracle_prefill_sample(2048)
     t = time.perf_counter(); pre(); tp = time.perf_counter() - t
@@ -508,6 +560,17 @@ def main():
         "value": world * sl_bytes / (sl_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_call": sl_ms,
         "tokens_per_s": world * SLOTS_CASE.batch * SLOTS_CASE.tokens / (sl_ms * 1e-3),
         "hbm_frac": sl_bytes / (sl_ms * 1e-3) / 1e9 / peaks["hbm"]}
+    cp_ms = max_over_ranks(conv_prefill_region(gdn, pre, stream), world)
+    cd_ms = max_over_ranks(conv_decode_region(gdn, dec, stream), world)
+    conv_state_b = CASE_DECODE.batch * (CONV_WIDTH - 1) * conv_channels(16, hv) * 2
+    cd_bytes = dbytes + 2 * conv_state_b
+    line["conv"] = {
+        "workload": "causal conv1d (width 4) + SiLU on q | k | v fused ahead of the core",
+        "prefill_ms_per_call": cp_ms, "prefill_tokens_per_s": world * T / (cp_ms * 1e-3),
+        "prefill_overhead_vs_plain": cp_ms / pre_mean - 1.0,
+        "decode_ms_per_call": cd_ms, "decode_gbs": cd_bytes / (cd_ms * 1e-3) / 1e9,
+        "decode_hbm_frac": cd_bytes / (cd_ms * 1e-3) / 1e9 / peaks["hbm"],
+        "decode_overhead_vs_plain": cd_ms / dec_mean - 1.0}
     if not args.no_e2e:
         e2e_ms, h2d, d2h = e2e_region(gdn, x, dec_y, dev, max(10, min(args.steps, 200)),
                                       3, stream)

@@ -26,7 +26,7 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED",
                 6: "GDN_ERR_WORKSPACE"}
 EXPORTED = ("gdn_status_string", "gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_decode",
             "gdn_check_device_status", "gdn_prefill_noalloc", "gdn_decode_slots", "gdn_prefill_strided",
-            "gdn_decode_strided")
+            "gdn_decode_strided", "gdn_prefill_conv", "gdn_decode_conv")
 
 
 class GdnError(RuntimeError):
@@ -47,6 +47,11 @@ class Stride(ctypes.Structure):
 
 class Strides(ctypes.Structure):
     _fields_ = [("q", Stride), ("k", Stride), ("v", Stride), ("z", Stride), ("a", Stride), ("b", Stride)]
+
+
+class Conv(ctypes.Structure):
+    _fields_ = [("width", ctypes.c_int32), ("weight", ctypes.c_void_p), ("state_in", ctypes.c_void_p),
+                ("state_out", ctypes.c_void_p)]
 
 
 def load(path: Optional[str] = None):
@@ -83,6 +88,13 @@ def load(path: Optional[str] = None):
             lib.gdn_decode_strided.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Strides), ctypes.c_int32,
                                                ctypes.c_int32, P, P, P, P, P, P, P, P, P, P, P, f32, P, P]
             lib.gdn_decode_strided.restype = ctypes.c_int
+            lib.gdn_prefill_conv.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Strides), ctypes.POINTER(Conv),
+                                             P, P, P, P, P, P, P, P, P, P, P, f32, P, P, P, sz, P]
+            lib.gdn_prefill_conv.restype = ctypes.c_int
+            lib.gdn_decode_conv.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Strides), ctypes.POINTER(Conv),
+                                            ctypes.c_int32, ctypes.c_int32, P, P, P, P, P, P, P, P, P, P, P, f32,
+                                            P, P]
+            lib.gdn_decode_conv.restype = ctypes.c_int
             lib.gdn_check_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
             lib.gdn_check_device_status.restype = ctypes.c_int
             _lib = lib
@@ -170,9 +182,25 @@ def alloc_workspace(num_seqs: int, total_tokens: int, hk: int, hv: int, device) 
     return buf[off:off + n] if n else buf[:0]
 
 
+def _conv(weight, state_in, state_out, dev):
+    """The conv descriptor of gdn_conv_t (weight [C, K] bf16, states [rows, K-1, C] bf16)."""
+    if weight.dim() != 2:
+        raise ValueError("conv_weight must be [channels, width]")
+    bf = torch.bfloat16
+    return Conv(int(weight.shape[1]), _ptr(weight, bf, "conv_weight", dev), _ptr(state_in, bf, "conv_state", dev),
+                _ptr(state_out, bf, "conv_state_out", dev))
+
+
 def prefill(q, k, v, a, b, A_log, dt_bias, cu_seqlens, init_state=None, z=None, norm_w=None,
-            eps: float = 1e-6, out=None, final_state=None, workspace=None, stream=None):
-    """Chunked GDN prefill through ``gdn_prefill``.  Returns (out, final_state).
+            eps: float = 1e-6, out=None, final_state=None, workspace=None, stream=None,
+            conv_weight=None, conv_state=None, conv_state_out=None):
+    """Chunked GDN prefill through ``gdn_prefill``.  Returns (out, final_state),
+    or (out, final_state, conv_state_out) when ``conv_weight`` is given.
+
+    With ``conv_weight`` [Hk*128 + Hk*128 + Hv*128, K] bf16 the causal conv1d
+    + SiLU runs on q | k | v ahead of the core (``gdn_prefill_conv``), from
+    ``conv_state`` [N, K-1, C] bf16 (None: zeros); ``conv_state_out`` (may be
+    ``conv_state`` itself) receives each sequence's last K-1 raw inputs.
 
     q, k [T, Hk, 128] bf16; v [T, Hv, 128] bf16; a, b [T, Hv] bf16 (dense,
     or views with a contiguous innermost dimension, e.g. slices of one packed
@@ -199,6 +227,15 @@ def prefill(q, k, v, a, b, A_log, dt_bias, cu_seqlens, init_state=None, z=None, 
             _in_ptr(z, "z", dev), _ptr(norm_w, bf, "norm_w", dev), float(eps), _ptr(out, bf, "out", dev),
             _ptr(final_state, f32, "final_state", dev), _ptr(workspace, torch.uint8, "workspace", dev),
             int(workspace.numel()), _stream_handle(stream, dev))
+    if conv_weight is not None:
+        K = int(conv_weight.shape[1])
+        if conv_state_out is None:
+            conv_state_out = torch.empty(N, K - 1, conv_weight.shape[0], dtype=torch.bfloat16, device=dev)
+        conv = _conv(conv_weight, conv_state, conv_state_out, dev)
+        code = load().gdn_prefill_conv(ctypes.byref(shape), None if strides is None else ctypes.byref(strides),
+                                       ctypes.byref(conv), *ins, *rest)
+        _check(code)
+        return out, final_state, conv_state_out
     if strides is None:
         code = load().gdn_prefill(ctypes.byref(shape), *ins, *rest)
     else:
@@ -256,9 +293,12 @@ def decode(q, k, v, a, b, A_log, dt_bias, state, z=None, norm_w=None, eps: float
 
 
 def decode_slots(q, k, v, a, b, A_log, dt_bias, state_pool, state_idx=None, z=None, norm_w=None,
-                 eps: float = 1e-6, out=None, stream=None):
+                 eps: float = 1e-6, out=None, stream=None, conv_weight=None, conv_state=None):
     """``tokens`` consecutive tokens per sequence through ``gdn_decode_slots``;
-    the pool slots named by ``state_idx`` are updated in place.
+    the pool slots named by ``state_idx`` are updated in place.  With
+    ``conv_weight`` [C, K] bf16 the causal conv1d + SiLU runs ahead of the
+    core (``gdn_decode_conv``) and ``conv_state`` [P, K-1, C] bf16, a pool
+    indexed like ``state_pool``, is rolled in place.
 
     q, k [B, T, Hk, 128] bf16; v [B, T, Hv, 128] bf16; a, b [B, T, Hv] bf16;
     state_pool [P, Hv, 128, 128] fp32; state_idx [B] int32 (device) or None
@@ -278,7 +318,11 @@ def decode_slots(q, k, v, a, b, A_log, dt_bias, state_pool, state_idx=None, z=No
             _ptr(state_pool, f32, "state_pool", dev), _ptr(state_idx, torch.int32, "state_idx", dev),
             _in_ptr(z, "z", dev), _ptr(norm_w, bf, "norm_w", dev), float(eps), _ptr(out, bf, "out", dev),
             _stream_handle(stream, dev))
-    if strides is None:
+    if conv_weight is not None:
+        conv = _conv(conv_weight, conv_state, conv_state, dev)
+        code = load().gdn_decode_conv(ctypes.byref(shape), None if strides is None else ctypes.byref(strides),
+                                      ctypes.byref(conv), int(T), int(state_pool.shape[0]), *ins, *rest)
+    elif strides is None:
         code = load().gdn_decode_slots(ctypes.byref(shape), int(T), int(state_pool.shape[0]), *ins, *rest)
     else:
         code = load().gdn_decode_strided(ctypes.byref(shape), ctypes.byref(strides), int(T),

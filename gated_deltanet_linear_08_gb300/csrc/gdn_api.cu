@@ -87,6 +87,36 @@ size_t span(const void *p, size_t tokens, size_t heads, const gdn::Stride &x, si
     return ((tokens - 1) * (size_t)x.t + (heads - 1) * (size_t)x.h + row) * 2;
 }
 
+// The caller's conv descriptor (NULL: no conv), checked against the shape.
+// `rows` is the number of state rows: sequences for prefill, slots for
+// decode.  state_out may equal state_in; any other overlap is rejected.
+gdn_status_t resolve_conv(const gdn_conv_t *c, const gdn_shape_t *s, size_t rows, bool decode,
+                          gdn::ConvArgs &o, size_t &state_bytes)
+{
+    o = gdn::ConvArgs{};
+    state_bytes = 0;
+    if (!c)
+        return GDN_OK;
+    if (c->width < 1 || c->width > 4 || !c->weight)
+        return GDN_ERR_INVALID_ARG;
+    if (decode && c->width > 1 && !c->state_in)
+        return GDN_ERR_INVALID_ARG;   // the slot pool holds the history
+    o.width = c->width;
+    o.channels = (2 * s->hk + s->hv) * 128;
+    o.weight = static_cast<const __nv_bfloat16 *>(c->weight);
+    o.state_in = static_cast<const __nv_bfloat16 *>(c->state_in);
+    o.state_out = static_cast<__nv_bfloat16 *>(c->state_out);
+    if (!aligned(c->weight, 2) || !aligned(c->state_in, 16) || !aligned(c->state_out, 16))
+        return GDN_ERR_ALIGNMENT;
+    state_bytes = rows * (size_t)(c->width - 1) * (size_t)o.channels * 2;
+    if (c->state_in != c->state_out && overlaps(c->state_in, state_bytes, c->state_out, state_bytes))
+        return GDN_ERR_INVALID_ARG;
+    const size_t wb = (size_t)o.channels * c->width * 2;
+    if (overlaps(c->state_out, state_bytes, c->weight, wb))
+        return GDN_ERR_INVALID_ARG;
+    return GDN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -112,11 +142,11 @@ size_t gdn_prefill_workspace_bytes(const gdn_shape_t *s)
     return gdn::prefill_workspace_bytes(s->num_seqs, s->total_tokens, s->hk, s->hv);
 }
 
-gdn_status_t gdn_prefill_strided(const gdn_shape_t *s, const gdn_strides_t *strides, const void *q,
-                                 const void *k, const void *v, const void *a, const void *b, const float *A_log,
-                                 const float *dt_bias, const float *init_state, const int32_t *cu_seqlens,
-                                 const void *z, const void *norm_w, float eps, void *out, float *final_state,
-                                 void *workspace, size_t workspace_bytes, void *stream)
+gdn_status_t gdn_prefill_conv(const gdn_shape_t *s, const gdn_strides_t *strides, const gdn_conv_t *conv,
+                              const void *q, const void *k, const void *v, const void *a, const void *b,
+                              const float *A_log, const float *dt_bias, const float *init_state,
+                              const int32_t *cu_seqlens, const void *z, const void *norm_w, float eps, void *out,
+                              float *final_state, void *workspace, size_t workspace_bytes, void *stream)
 {
     gdn_status_t st = check_shape(s);
     if (st != GDN_OK)
@@ -160,6 +190,21 @@ gdn_status_t gdn_prefill_strided(const gdn_shape_t *s, const gdn_strides_t *stri
         return GDN_ERR_INVALID_ARG;   // partial overlap; exact equality is the in-place case
     if (overlaps(final_state, st_b, out, out_b) || overlaps(final_state, st_b, workspace, need))
         return GDN_ERR_INVALID_ARG;
+    gdn::ConvArgs cv;
+    size_t cs_b = 0;
+    if ((st = resolve_conv(conv, s, N, false, cv, cs_b)) != GDN_OK)
+        return st;
+    if (cv.state_out) {
+        // the state written must not alias anything the call reads or writes
+        for (const auto &x : ins)
+            if (overlaps(cv.state_out, cs_b, x.p, x.n))
+                return GDN_ERR_INVALID_ARG;
+        if (overlaps(cv.state_out, cs_b, out, out_b) || overlaps(cv.state_out, cs_b, final_state, st_b))
+            return GDN_ERR_INVALID_ARG;
+    }
+    if (overlaps(cv.state_in, cs_b, out, out_b) || overlaps(cv.state_in, cs_b, final_state, st_b)
+        || overlaps(cv.state_in, cs_b, workspace, need))
+        return GDN_ERR_INVALID_ARG;
 
     gdn::PrefillArgs p{};
     p.num_seqs = s->num_seqs;
@@ -168,6 +213,7 @@ gdn_status_t gdn_prefill_strided(const gdn_shape_t *s, const gdn_strides_t *stri
     p.hv = s->hv;
     p.max_chunks = gdn::prefill_max_chunks(s->num_seqs, s->total_tokens);
     p.in = in;
+    p.conv = cv;
     p.q = q; p.k = k; p.v = v; p.a = a; p.b = b;
     p.A_log = A_log; p.dt_bias = dt_bias;
     p.init_state = init_state;
@@ -182,6 +228,16 @@ gdn_status_t gdn_prefill_strided(const gdn_shape_t *s, const gdn_strides_t *stri
     return gdn::launch_prefill(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+gdn_status_t gdn_prefill_strided(const gdn_shape_t *s, const gdn_strides_t *strides, const void *q,
+                                 const void *k, const void *v, const void *a, const void *b, const float *A_log,
+                                 const float *dt_bias, const float *init_state, const int32_t *cu_seqlens,
+                                 const void *z, const void *norm_w, float eps, void *out, float *final_state,
+                                 void *workspace, size_t workspace_bytes, void *stream)
+{
+    return gdn_prefill_conv(s, strides, nullptr, q, k, v, a, b, A_log, dt_bias, init_state, cu_seqlens, z, norm_w,
+                            eps, out, final_state, workspace, workspace_bytes, stream);
+}
+
 gdn_status_t gdn_prefill(const gdn_shape_t *s, const void *q, const void *k, const void *v,
                          const void *a, const void *b, const float *A_log, const float *dt_bias,
                          const float *init_state, const int32_t *cu_seqlens, const void *z,
@@ -192,11 +248,11 @@ gdn_status_t gdn_prefill(const gdn_shape_t *s, const void *q, const void *k, con
                                eps, out, final_state, workspace, workspace_bytes, stream);
 }
 
-gdn_status_t gdn_decode_strided(const gdn_shape_t *s, const gdn_strides_t *strides, int32_t tokens,
-                                int32_t num_slots, const void *q, const void *k, const void *v, const void *a,
-                                const void *b, const float *A_log, const float *dt_bias, float *state,
-                                const int32_t *state_idx, const void *z, const void *norm_w, float eps,
-                                void *out, void *stream)
+gdn_status_t gdn_decode_conv(const gdn_shape_t *s, const gdn_strides_t *strides, const gdn_conv_t *conv,
+                             int32_t tokens, int32_t num_slots, const void *q, const void *k, const void *v,
+                             const void *a, const void *b, const float *A_log, const float *dt_bias, float *state,
+                             const int32_t *state_idx, const void *z, const void *norm_w, float eps, void *out,
+                             void *stream)
 {
     gdn_status_t st = check_shape(s);
     if (st != GDN_OK)
@@ -236,6 +292,19 @@ gdn_status_t gdn_decode_strided(const gdn_shape_t *s, const gdn_strides_t *strid
     for (const auto &x : ins)
         if (overlaps(out, out_b, x.p, x.n))
             return GDN_ERR_INVALID_ARG;
+    gdn::ConvArgs cv;
+    size_t cs_b = 0;
+    if ((st = resolve_conv(conv, s, (size_t)num_slots, true, cv, cs_b)) != GDN_OK)
+        return st;
+    if (conv) {
+        // neither conv state may alias the outputs; the one written, nothing read
+        if (overlaps(out, out_b, cv.state_in, cs_b) || overlaps(out, out_b, cv.state_out, cs_b)
+            || overlaps(cv.state_in, cs_b, state, (size_t)num_slots * hv * 128 * 128 * 4))
+            return GDN_ERR_INVALID_ARG;
+        for (const auto &x : ins)
+            if (overlaps(cv.state_out, cs_b, x.p, x.n))
+                return GDN_ERR_INVALID_ARG;
+    }
 
     gdn::DecodeArgs p{};
     p.batch = s->num_seqs;
@@ -245,6 +314,7 @@ gdn_status_t gdn_decode_strided(const gdn_shape_t *s, const gdn_strides_t *strid
     p.num_slots = num_slots;
     p.state_idx = state_idx;
     p.in = in;
+    p.conv = cv;
     p.q = q; p.k = k; p.v = v; p.a = a; p.b = b;
     p.A_log = A_log; p.dt_bias = dt_bias;
     p.state = state;
@@ -254,6 +324,16 @@ gdn_status_t gdn_decode_strided(const gdn_shape_t *s, const gdn_strides_t *strid
     if (!p.status)
         return GDN_ERR_CUDA;
     return gdn::launch_decode(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status_t gdn_decode_strided(const gdn_shape_t *s, const gdn_strides_t *strides, int32_t tokens,
+                                int32_t num_slots, const void *q, const void *k, const void *v, const void *a,
+                                const void *b, const float *A_log, const float *dt_bias, float *state,
+                                const int32_t *state_idx, const void *z, const void *norm_w, float eps,
+                                void *out, void *stream)
+{
+    return gdn_decode_conv(s, strides, nullptr, tokens, num_slots, q, k, v, a, b, A_log, dt_bias, state, state_idx,
+                           z, norm_w, eps, out, stream);
 }
 
 gdn_status_t gdn_decode_slots(const gdn_shape_t *s, int32_t tokens, int32_t num_slots, const void *q,

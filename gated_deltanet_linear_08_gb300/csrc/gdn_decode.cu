@@ -16,7 +16,9 @@
 // token): loads and stores are 16-byte, warp-contiguous rows of 512 bytes,
 // marked streaming so they do not displace other data in L2.
 #include "common.cuh"
+#include "conv.cuh"
 #include "kernels.h"
+#include "tc05.cuh"
 
 namespace gdn {
 namespace {
@@ -25,7 +27,10 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRowsPerThread = kD / kWarps;  // 16
 
-template <bool kNorm>
+// KW: width of the causal conv ahead of the core (0: none).  Warps 0-2 keep,
+// per lane, the conv weights and the K-1 previous raw inputs of their four
+// k, q or v channels in registers across the tokens.
+template <bool kNorm, int KW>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_kernel(DecodeArgs p)
 {
@@ -63,6 +68,46 @@ decode_kernel(DecodeArgs p)
     for (int i = 0; i < kRowsPerThread; ++i)
         st[i] = __ldcs(reinterpret_cast<const float4 *>(S + (size_t)(warp + kWarps * i) * kD) + lane);
 
+    // conv channels of this lane (warps 0-2: k, q, v), weights and history
+    constexpr int kHist = KW > 1 ? KW - 1 : 1;
+    float cw[KW > 0 ? KW : 1][4], win[kHist][4];
+    if constexpr (KW > 0) {
+        if (warp < 3) {
+            const int chan = (warp == 0 ? (hk + hq) * kD : warp == 1 ? hq * kD : (2 * hk + h) * kD) + lane * 4;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+#pragma unroll
+                for (int j = 0; j < KW; ++j)
+                    cw[j][e] = bf2f(p.conv.weight[(size_t)(chan + e) * KW + j]);
+#pragma unroll
+            for (int j = 0; j < KW - 1; ++j) {
+                const uint2 u = *reinterpret_cast<const uint2 *>(
+                    p.conv.state_in + (((size_t)slot * (KW - 1) + j) * p.conv.channels + chan));
+                win[j][0] = __uint_as_float(u.x << 16); win[j][1] = __uint_as_float(u.x & 0xFFFF0000u);
+                win[j][2] = __uint_as_float(u.y << 16); win[j][3] = __uint_as_float(u.y & 0xFFFF0000u);
+            }
+        }
+    }
+    // raw token inputs -> conv + SiLU, rounded to bf16; the window moves on
+    auto conv4 = [&](float (&f)[4]) {
+        if constexpr (KW > 0) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float acc = cw[KW - 1][e] * f[e];
+#pragma unroll
+                for (int j = 0; j < KW - 1; ++j)
+                    acc = fmaf(cw[j][e], win[j][e], acc);
+                if constexpr (KW > 1) {
+#pragma unroll
+                    for (int j = 0; j + 1 < KW - 1; ++j)
+                        win[j][e] = win[j + 1][e];
+                    win[KW - 2][e] = f[e];
+                }
+                f[e] = bf16_round(silu_f(acc));
+            }
+        }
+    };
+
     const float scale = rsqrtf((float)kD);
     for (int t = 0; t < T; ++t) {
         const size_t tok = (size_t)n * T + t;
@@ -75,6 +120,7 @@ decode_kernel(DecodeArgs p)
             const uint2 u = *reinterpret_cast<const uint2 *>(src);
             float f[4] = {__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
                           __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u)};
+            conv4(f);
             float ss = f[0] * f[0] + f[1] * f[1] + f[2] * f[2] + f[3] * f[3];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1)
@@ -88,10 +134,12 @@ decode_kernel(DecodeArgs p)
             const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(p.v)
                                        + (int64_t)tok * p.in.v.t + (int64_t)h * p.in.v.h + lane * 4;
             const uint2 u = *reinterpret_cast<const uint2 *>(src);
-            s_v[lane * 4 + 0] = __uint_as_float(u.x << 16);
-            s_v[lane * 4 + 1] = __uint_as_float(u.x & 0xFFFF0000u);
-            s_v[lane * 4 + 2] = __uint_as_float(u.y << 16);
-            s_v[lane * 4 + 3] = __uint_as_float(u.y & 0xFFFF0000u);
+            float f[4] = {__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                          __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u)};
+            conv4(f);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                s_v[lane * 4 + j] = f[j];
         } else if (warp == 3 && lane == 0) {
             const float av = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.a)[(int64_t)tok * p.in.a.t + (int64_t)h * p.in.a.h]);
             const float bv = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.b)[(int64_t)tok * p.in.b.t + (int64_t)h * p.in.b.h]);
@@ -183,6 +231,43 @@ decode_kernel(DecodeArgs p)
         __stcs(reinterpret_cast<float4 *>(S + (size_t)(warp + kWarps * i) * kD) + lane, st[i]);
 }
 
+// The conv-state roll after a decode call: one thread per 8 channels of a
+// sequence's slot.  It runs once the decode grid has finished (every value
+// head of a group reads the same q and k history, so none of it may change
+// while any of them still runs).
+constexpr int kRollThreads = 128;
+
+__global__ void __launch_bounds__(kRollThreads)
+conv_roll_kernel(DecodeArgs p)
+{
+    grid_dep_wait();
+    const int n = blockIdx.y;
+    const int c = (blockIdx.x * kRollThreads + threadIdx.x) * 8;
+    if (c >= p.conv.channels)
+        return;
+    int slot = n;
+    if (p.state_idx) {
+        slot = p.state_idx[n];
+        if (slot >= p.num_slots)
+            return;
+    }
+    if (slot < 0)
+        return;
+    conv_roll8(p.conv, p.q, p.k, p.v, p.in, p.hk, c, slot, slot, (int64_t)n * p.tokens, p.tokens);
+}
+
+template <bool kNorm>
+void launch_width(const DecodeArgs &args, dim3 grid, cudaStream_t stream)
+{
+    switch (args.conv.width) {
+    case 1: decode_kernel<kNorm, 1><<<grid, kThreads, 0, stream>>>(args); break;
+    case 2: decode_kernel<kNorm, 2><<<grid, kThreads, 0, stream>>>(args); break;
+    case 3: decode_kernel<kNorm, 3><<<grid, kThreads, 0, stream>>>(args); break;
+    case 4: decode_kernel<kNorm, 4><<<grid, kThreads, 0, stream>>>(args); break;
+    default: decode_kernel<kNorm, 0><<<grid, kThreads, 0, stream>>>(args);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs &args, cudaStream_t stream)
@@ -191,10 +276,23 @@ cudaError_t launch_decode(const DecodeArgs &args, cudaStream_t stream)
         return cudaSuccess;
     dim3 grid(args.hv, args.batch);
     if (args.z)
-        decode_kernel<true><<<grid, kThreads, 0, stream>>>(args);
+        launch_width<true>(args, grid, stream);
     else
-        decode_kernel<false><<<grid, kThreads, 0, stream>>>(args);
-    return cudaGetLastError();
+        launch_width<false>(args, grid, stream);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || args.conv.width <= 1 || !args.conv.state_out)
+        return e;
+    // launched early behind the decode grid; it waits for that grid's end
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((args.conv.channels / 8 + kRollThreads - 1) / kRollThreads, args.batch);
+    cfg.blockDim = dim3(kRollThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, conv_roll_kernel, args);
 }
 
 }  // namespace gdn

@@ -23,8 +23,10 @@
 //               32 (w % 4) .. +31 and value columns 16 (w / 4) .. +15
 //   warp 8      issues every MMA and the copy of S to the workspace
 //   warp 9      issues the stage copies (four stages: Mc, this CTA's Bc
-//               slice, e^{G_last})
+//               slice, e^{G_last}), then rolls this CTA's share of the
+//               carried conv state
 #include "common.cuh"
+#include "conv.cuh"
 #include "kernels.h"
 #include "tc05.cuh"
 
@@ -219,6 +221,18 @@ scan_kernel(PrefillArgs p)
             }
         }
         __syncwarp();
+        // The carried conv state.  Every prep CTA has read the old one (the
+        // dependency wait above), so it may be rewritten in place.  This CTA
+        // rolls its value slice of head h and, for the first value head of a
+        // group, the same slice of q and k head h / group.
+        if (p.conv.width > 1 && p.conv.state_out) {
+            const int grp = hv / p.hk, hq = h / grp;
+            if (lane < (h % grp == 0 ? 12 : 4)) {
+                const int part = lane >> 2, c = r * kNv + (lane & 3) * 8;
+                const int chan = part == 0 ? (2 * p.hk + h) * kD + c : part == 1 ? hq * kD + c : (p.hk + hq) * kD + c;
+                conv_roll8(p.conv, p.q, p.k, p.v, p.in, p.hk, chan, n, n, tok0, len);
+            }
+        }
     } else {
         // ------------------------------------------------------------ state
         const int q = warp & 3, cg = warp >> 2;

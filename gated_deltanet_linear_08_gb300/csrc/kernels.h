@@ -5,6 +5,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 namespace gdn {
@@ -19,12 +20,23 @@ struct InputStrides {
     Stride q, k, v, z, a, b;
 };
 
+// Causal conv1d + SiLU over the q | k | v channels ahead of the core
+// (width 0: none).  state_in / state_out: bf16 [rows][width-1][channels].
+struct ConvArgs {
+    int width;
+    int channels;               // Hk*128 + Hk*128 + Hv*128
+    const __nv_bfloat16 *weight;   // [channels][width]
+    const __nv_bfloat16 *state_in;
+    __nv_bfloat16 *state_out;
+};
+
 struct DecodeArgs {
     int batch, hk, hv;
     int tokens;                    // consecutive tokens per sequence (1..8)
     int num_slots;                 // slots in the state pool
     const int32_t *state_idx;      // slot per sequence, or null for slot n
     InputStrides in;
+    ConvArgs conv;
     const void *q, *k, *v, *a, *b;
     const float *A_log, *dt_bias;
     float *state;                  // state pool [num_slots, hv, 128, 128]
@@ -38,6 +50,7 @@ struct PrefillArgs {
     int num_seqs, total_tokens, hk, hv;
     int max_chunks;                // upper bound on chunks: ceil(T/64) + N
     InputStrides in;
+    ConvArgs conv;
     const void *q, *k, *v, *a, *b;
     const float *A_log, *dt_bias;
     const float *init_state;

@@ -183,6 +183,25 @@ def make_decode_slots_inputs(case: DecodeSlotsCase) -> dict:
                 z=z, norm_w=w, eps=case.eps, hk=hk, hv=hv, d=d, batch=B, tokens=T, slots=P)
 
 
+def conv_channels(hk: int, hv: int, d: int = D_HEAD) -> int:
+    """Channels of the short conv ahead of the core: q | k | v."""
+    return (2 * hk + hv) * d
+
+
+def make_conv_inputs(channels: int, width: int, rows: int, seed: int = 0, state: bool = True) -> dict:
+    """Weights and carried states of the causal conv, from a generator of their
+    own (so the core's inputs of a case do not change with the conv).  Draw
+    order: weight [C, K] ~ U(-1/sqrt(K), 1/sqrt(K)) (the default fan-in bound
+    of a depthwise conv), rounded to bf16; then, if ``state``, the carried raw
+    inputs [rows, K-1, C] ~ N(0, 1) rounded to bf16, like the projections."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(10_000 + seed)
+    bound = 1.0 / float(width) ** 0.5
+    w = _bf16(torch.empty(channels, width).uniform_(-bound, bound, generator=g))
+    st = _bf16(torch.randn(rows, width - 1, channels, generator=g)) if state else None
+    return dict(weight=w, state=st, width=width, channels=channels)
+
+
 # The workloads of the contract: the Qwen3.5-4B geometry (16/16/32/128) at
 # T=64, 8x128 packed, T=2048 with the gated-RMSNorm epilogue, the Hv=48 varlen
 # family member, and batch-256 decode over 64 steps.

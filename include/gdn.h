@@ -232,6 +232,65 @@ gdn_status_t gdn_decode_strided(const gdn_shape_t *shape, const gdn_strides_t *s
                                 const void *z, const void *norm_w, float eps,
                                 void *out, void *stream);
 
+/*
+ * Causal conv1d + SiLU ahead of the core, fused into it (the JevAny page,
+ * "Add opt-in fused Qwen3.5 inference kernels", Measurements, lists
+ * causal-conv1d among the path's dependencies; its definition here is a
+ * reading).  Over the C = Hk*128 + Hk*128 + Hv*128 channels q | k | v of
+ * each token (each head 128 contiguous channels), with K = width taps:
+ *     y[t, c] = silu( sum_j weight[c][j] * x[t - (K-1) + j, c] )
+ * computed in fp32, rounded to bf16; the core runs on y.  Positions before a
+ * sequence's first token come from its carried state: the K-1 raw inputs
+ * that preceded it, oldest first.  z is not convolved.
+ *   width     1..4
+ *   weight    bf16 [C][width], 2-byte aligned
+ *   state_in  bf16 [rows][K-1][C], 16-byte aligned: one row per sequence for
+ *             prefill (rows = N; NULL means zeros), the slot pool for decode
+ *             (rows = num_slots, sequence n at its slot; required if K > 1)
+ *   state_out same layout: each sequence's last K-1 raw inputs after the call
+ *             (for a sequence shorter than K-1, the tail of the old state
+ *             followed by its tokens; an empty sequence copies its row).
+ *             NULL skips it; it may equal state_in (updated in place) or lie
+ *             apart from it; decode writes only the slots it names.
+ * Errors: width outside 1..4 or a NULL weight, or a NULL decode state_in with
+ * K > 1 -> GDN_ERR_INVALID_ARG; misaligned pointers -> GDN_ERR_ALIGNMENT;
+ * state_out partially overlapping state_in, or either overlapping an output,
+ * the recurrent states or the workspace -> GDN_ERR_INVALID_ARG.
+ */
+typedef struct {
+    int32_t width;
+    const void *weight;
+    const void *state_in;
+    void *state_out;
+} gdn_conv_t;
+
+/* gdn_prefill_strided with the conv ahead of the core; conv == NULL is
+ * gdn_prefill_strided. */
+gdn_status_t gdn_prefill_conv(const gdn_shape_t *shape, const gdn_strides_t *strides,
+                              const gdn_conv_t *conv,
+                              const void *q, const void *k, const void *v,
+                              const void *a, const void *b,
+                              const float *A_log, const float *dt_bias,
+                              const float *init_state, const int32_t *cu_seqlens,
+                              const void *z, const void *norm_w, float eps,
+                              void *out, float *final_state,
+                              void *workspace, size_t workspace_bytes,
+                              void *stream);
+
+/* gdn_decode_strided with the conv ahead of the core; conv->state_in is the
+ * conv-state pool, indexed like state_pool.  Skipped and out-of-pool
+ * sequences leave their conv state untouched.  With conv->state_out set,
+ * a second small kernel rolls the states once the decode grid has finished
+ * (the heads of a group share their q and k history). */
+gdn_status_t gdn_decode_conv(const gdn_shape_t *shape, const gdn_strides_t *strides,
+                             const gdn_conv_t *conv, int32_t tokens, int32_t num_slots,
+                             const void *q, const void *k, const void *v,
+                             const void *a, const void *b,
+                             const float *A_log, const float *dt_bias,
+                             float *state_pool, const int32_t *state_idx,
+                             const void *z, const void *norm_w, float eps,
+                             void *out, void *stream);
+
 /* Reads and clears the device status word that kernels set when a bounded
  * wait runs out.  Synchronises the device: not for the hot path.  Returns
  * GDN_OK, GDN_ERR_DEVICE_STATUS (and the raw bits in *bits when non-NULL),

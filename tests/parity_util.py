@@ -86,3 +86,107 @@ def assert_state_close(got, ref, what="state", scale_with_ref=False):
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
     assert s["violations"] == 0, f"{what}: bound {bound}: {s}"
     return s
+
+
+# ---------------------------------------------------------------------------
+# The causal conv ahead of the core rounds its output to bf16.  The kernels
+# evaluate it in fp32 (exact bf16 products, fp32 sums, fast exp and divide),
+# the oracle in fp64: where the exact value lies on a bf16 rounding midpoint
+# the two may round apart, one bf16 ulp in one input of the core.  That is a
+# quantisation decision, so the parity inputs are moved off such ties: any
+# output whose fp64 value lies within 2^-20 (|y| + sum_j |w_j x_j|) of a
+# midpoint (16x the fp32 evaluation error, which is below K 2^-24 of the
+# sum of magnitudes plus a few fp32 ulps of the SiLU) has the raw input of
+# its own token nudged by a few bf16 ulps, until none is left.  Outputs
+# whose bf16 ulp is below 2^-16 are left alone: near zero the fp32 sum's
+# cancellation error can reach their ulp whatever the input, but a flip there
+# moves that input by at most 2^-16, which moves a decode state element by
+# at most beta |kn_i| 2^-16 <= 1.5e-5 (kn has unit norm), an order below the
+# state bound.  On such inputs both sides round every conv output that
+# matters the same way, and the core's bounds apply unchanged.
+TIE_REL = 2.0 ** -20
+TIE_MIN_ULP = 2.0 ** -16
+
+
+def conv_ties(x, w, state, ts=None, cs=None):
+    """Outputs of one sequence's conv too close to a bf16 rounding midpoint:
+    x [T, C], w [C, K], state [K-1, C] or None (fp64).  Returns a [T, C] mask,
+    or, given output positions ts, cs, the mask at those positions only."""
+    T, C = x.shape
+    K = w.shape[1]
+    prev = np.zeros((K - 1, C)) if state is None else state
+    xe = np.concatenate([prev, x], axis=0)
+    if ts is None:
+        win = np.stack([xe[j:j + T] for j in range(K)], axis=-1)        # [T, C, K]
+        wk = w[None, :, :]
+    else:
+        win = xe[ts[:, None] + np.arange(K)[None, :], cs[:, None]]     # [n, K]
+        wk = w[cs]
+    terms = wk * win
+    acc, mag = terms.sum(axis=-1), np.abs(terms).sum(axis=-1)
+    y = oracle.silu(acc)
+    _, e = np.frexp(y)
+    ulp = np.ldexp(1.0, e - 8)               # bf16: 8 significant bits
+    mid = np.floor(y / ulp) * ulp + 0.5 * ulp
+    return (np.abs(y - mid) <= TIE_REL * (np.abs(y) + mag)) & (ulp >= TIE_MIN_ULP)
+
+
+def conv_nudge_off_ties(X, cu, w, states, max_iter: int = 40) -> int:
+    """X: bf16 [T_total, C] raw q | k | v rows of packed sequences, cu:
+    sequence starts, w: bf16 [C, K], states: per sequence a bf16 [K-1, C]
+    tensor (a view into the carried states) or None.  For each tie, the input
+    in the output's window with the largest weight -- a token, or a carried
+    state row -- moves by a few bf16 ulps; X and the states change in place.
+    After the first pass only the outputs whose window saw a change are
+    checked again.  Returns the number of inputs nudged."""
+    wf = to_f64(w)
+    K = wf.shape[1]
+    nudged = 0
+
+    def bump(t, idx):
+        old = t[idx].float()
+        t[idx] = (old + old.abs() * 2.0 ** -5 + 2.0 ** -8).to(torch.bfloat16)
+
+    for n in range(len(cu) - 1):
+        s, e = int(cu[n]), int(cu[n + 1])
+        if e == s:
+            continue
+        st = states[n]
+        L = e - s
+        ts = cs = None
+        for _ in range(max_iter):
+            xf = X[s:e].double().numpy()
+            stf = None if st is None else to_f64(st)
+            mask = conv_ties(xf, wf, stf, ts, cs)
+            if ts is None:
+                ts, cs = np.nonzero(mask)
+            else:
+                ts, cs = ts[mask], cs[mask]
+            if ts.size == 0:
+                break
+            pos = ts[:, None] - (K - 1) + np.arange(K)[None, :]   # window positions
+            aw = np.abs(wf[cs])
+            if st is None:
+                aw = np.where(pos >= 0, aw, -1.0)
+            where = pos[np.arange(ts.size), np.argmax(aw, axis=1)]
+            tok = where >= 0
+            if tok.any():
+                bump(X, (torch.as_tensor(s + where[tok]), torch.as_tensor(cs[tok])))
+            if (~tok).any():
+                bump(st, (torch.as_tensor(K - 1 + where[~tok]), torch.as_tensor(cs[~tok])))
+            nudged += int(ts.size)
+            # outputs that read a changed input: positions where .. where+K-1
+            nt = (where[:, None] + np.arange(K)[None, :]).ravel()
+            nc = np.repeat(cs, K)
+            keep = (nt >= 0) & (nt < L)
+            pairs = np.unique(np.stack([nt[keep], nc[keep]], axis=1), axis=0)
+            ts, cs = pairs[:, 0], pairs[:, 1]
+        else:
+            raise AssertionError("conv inputs still on rounding ties after nudging")
+    return nudged
+
+
+def split_qkv(X, hk, hv, d=128):
+    T = X.shape[0]
+    return (X[:, :hk * d].reshape(T, hk, d).contiguous(), X[:, hk * d:2 * hk * d].reshape(T, hk, d).contiguous(),
+            X[:, 2 * hk * d:].reshape(T, hv, d).contiguous())

@@ -166,6 +166,42 @@ def test_strided_entry_points_reject_bad_strides(lib):
                                    FAKE + 64 * W, FAKE + 0xA0000000, FAKE + 0xB0000000, 1 << 30, None) == 1
 
 
+def test_conv_entry_points_reject_bad_descriptors(lib):
+    # host-side validation only: every call here fails before any launch
+    W, S = FAKE + 0xC0000000, FAKE + 0xD0000000
+    shape = B.make_shape(1, 64, 16, 32)
+
+    def pre(width=4, weight=W, sin=S, sout=S, out=FAKE + 0x80000000):
+        cv = B.Conv(width, weight, sin, sout)
+        return lib.gdn_prefill_conv(ctypes.byref(shape), None, ctypes.byref(cv), FAKE, FAKE + 0x10000000,
+                                    FAKE + 0x20000000, FAKE + 0x30000000, FAKE + 0x40000000, FAKE + 0x50000000,
+                                    FAKE + 0x60000000, None, FAKE + 0x70000000, None, None, 1e-6, out,
+                                    FAKE + 0x90000000, FAKE + 0xA0000000, 1 << 40, None)
+
+    def dec(width=4, weight=W, sin=S, sout=S):
+        cv = B.Conv(width, weight, sin, sout)
+        return lib.gdn_decode_conv(ctypes.byref(B.make_shape(4, 8, 16, 32)), None, ctypes.byref(cv), 2, 8, FAKE,
+                                   FAKE + 0x10000000, FAKE + 0x20000000, FAKE + 0x30000000, FAKE + 0x40000000,
+                                   FAKE + 0x50000000, FAKE + 0x60000000, FAKE + 0x70000000, None, None, None,
+                                   1e-6, FAKE + 0x90000000, None)
+    for call in (pre, dec):
+        assert call(width=0) == 1                    # width outside 1..4
+        assert call(width=5) == 1
+        assert call(weight=None) == 1
+        assert call(weight=W + 1) == 3               # bf16 weights need 2-byte alignment
+        assert call(sin=S + 8, sout=S + 8) == 3      # states need 16-byte alignment
+        assert call(sout=S + 4096) == 1              # partial overlap of the two states
+        assert call(sout=FAKE + 0x20000000) == 1     # written state over an input (v)
+    assert pre(sout=FAKE + 0x80000000) == 1          # over the output
+    assert pre(sout=FAKE + 0x90000000) == 1          # over the final states
+    assert dec(sin=None, sout=None) == 1             # decode needs the slot pool of conv states
+    assert dec(sout=FAKE + 0x70000000) == 1          # over the recurrent-state pool
+    assert dec(sin=FAKE + 0x90000000, sout=FAKE + 0x90000000) == 1   # over the output
+    # conv width 1 carries no state: NULL states are fine up to the launch,
+    # which the fake pointers never reach in the other cases either
+    assert pre(width=1, sin=None, sout=None, out=FAKE) == 1          # (out over q: still rejected)
+
+
 def test_missing_library_fails_loudly(tmp_path):
     saved = B._lib
     try:

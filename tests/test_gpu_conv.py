@@ -1,0 +1,267 @@
+"""GPU parity of the causal conv1d + SiLU fused ahead of the core (JevAny page
+"Add opt-in fused Qwen3.5 inference kernels", Measurements: causal-conv1d is
+one of the path's dependencies) against the fp64 oracle: oracle.conv_inputs
+(or causal_conv_silu per sequence) followed by oracle.prefill or one
+oracle.decode_step per token.
+
+The conv output is rounded to bf16 on both sides; the kernels sum in fp32 and
+the oracle in fp64, so an element whose value sits on a bf16 rounding
+midpoint may round the other way (one bf16 ulp in the core's input).  That
+rounding is a quantisation decision: the parity inputs are moved off such
+ties first (parity_util.conv_nudge_off_ties), after which the core's outputs
+and states are held to the same bounds as without the conv.  One prefill
+case runs on the seeded inputs as drawn, where the output bounds still hold.
+The carried conv states are raw inputs moved around, so they must match bit
+for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_deltanet_linear_08_gb300.inputs import (DecodeSlotsCase, PrefillCase, conv_channels, make_conv_inputs,
+                                                   make_decode_slots_inputs, make_prefill_inputs, to_f64)
+from parity_util import (DECODE_STATE_REL, assert_out_close, assert_state_close, conv_nudge_off_ties, split_qkv,
+                         to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_prefill_conv(x, cv):
+    qc, kc, vc, new = oracle.conv_inputs(x["cu_seqlens"].numpy(), to_f64(x["q"]), to_f64(x["k"]), to_f64(x["v"]),
+                                         to_f64(cv["weight"]), to_f64(cv["state"]))
+    f = {n: to_f64(x[n]) for n in ("a", "b", "A_log", "dt_bias", "init_state", "z", "norm_w")}
+    ro, rs = oracle.prefill(x["cu_seqlens"].numpy(), qc, kc, vc, f["a"], f["b"], f["A_log"], f["dt_bias"],
+                            f["init_state"], f["z"], f["norm_w"], eps=x["eps"])
+    return ro, rs, new
+
+
+def _gpu_prefill_conv(x, cv, in_place=False):
+    import gated_deltanet_linear_08_gb300 as gdn
+    d = to_dev(x)
+    w = cv["weight"].cuda()
+    st = None if cv["state"] is None else cv["state"].cuda()
+    out, fin, cs = gdn.prefill(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["cu_seqlens"],
+                               init_state=d["init_state"], z=d["z"], norm_w=d["norm_w"], eps=x["eps"],
+                               conv_weight=w, conv_state=st, conv_state_out=st if in_place else None)
+    torch.cuda.synchronize()
+    assert gdn.check_device_status() == 0
+    return out, fin, cs
+
+
+def _off_ties(x, cv):
+    """Nudge the raw q, k, v of a prefill case off conv rounding ties."""
+    T, hk, hv = x["q"].shape[0], x["q"].shape[1], x["v"].shape[1]
+    X = torch.cat([x["q"].reshape(T, -1), x["k"].reshape(T, -1), x["v"].reshape(T, -1)], dim=1)
+    N = len(x["seqlens"])
+    states = [None if cv["state"] is None else cv["state"][n] for n in range(N)]
+    nudged = conv_nudge_off_ties(X, x["cu_seqlens"].tolist(), cv["weight"], states)
+    x["q"], x["k"], x["v"] = split_qkv(X, hk, hv)
+    return nudged
+
+
+def _check_prefill(case, width, with_state=True, in_place=False, off_ties=True):
+    x = make_prefill_inputs(case)
+    cv = make_conv_inputs(conv_channels(case.hk, case.hv), width, len(x["seqlens"]), seed=case.seed,
+                          state=with_state)
+    if off_ties:
+        _off_ties(x, cv)
+    ro, rs, new = _oracle_prefill_conv(x, cv)
+    out, fin, cs = _gpu_prefill_conv(x, cv, in_place=in_place)
+    so = assert_out_close(out.double().cpu().numpy(), ro, case.name + " out")
+    ss = assert_state_close(fin.double().cpu().numpy(), rs, case.name + " state")
+    assert np.array_equal(cs.double().cpu().numpy(), new), case.name + " conv state"
+    print(case.name, "K", width, "out", so, "state", ss)
+    return x, cv, out, fin, cs
+
+
+def test_prefill_conv_ragged_with_short_sequences():
+    # lengths 1, 2 and 3 are shorter than or equal to K-1: their new conv state
+    # keeps part of the old one
+    # (on the inputs as drawn: no nudging off rounding ties)
+    _check_prefill(PrefillCase("conv_ragged", seqlens=[200, 64, 1, 2, 90, 130, 3], hk=2, hv=4, init_state=True,
+                               gated_norm=True, seed=41), 4, off_ties=False)
+
+
+@pytest.mark.parametrize("width", [1, 2, 3, 4])
+def test_prefill_conv_widths_grouped_heads(width):
+    _check_prefill(PrefillCase(f"conv_w{width}", seqlens=[70, 2, 129], hk=2, hv=6, init_state=True, seed=42),
+                   width)
+
+
+def test_prefill_conv_zero_state_and_empty_sequences():
+    _check_prefill(PrefillCase("conv_zero", seqlens=[0, 65, 0, 1, 128], hk=2, hv=4, seed=43), 4, with_state=False)
+    x, cv, *_ = _check_prefill(PrefillCase("conv_empty", seqlens=[0, 65, 0, 1], hk=2, hv=4, seed=44), 4)
+
+
+def test_prefill_conv_state_in_place_matches_out_of_place():
+    case = PrefillCase("conv_inplace", seqlens=[150, 2, 64], hk=2, hv=4, init_state=True, seed=45)
+    _, _, out_a, fin_a, cs_a = _check_prefill(case, 4)
+    _, _, out_b, fin_b, cs_b = _check_prefill(case, 4, in_place=True)
+    assert torch.equal(out_a, out_b) and torch.equal(fin_a, fin_b) and torch.equal(cs_a, cs_b)
+
+
+def test_prefill_conv_T2048_workload():
+    # the Qwen3.5-4B geometry at T=2048 with the gated RMSNorm, conv width 4
+    _check_prefill(PrefillCase("conv_T2048", seqlens=[2048], gated_norm=True, init_state=True, seed=46), 4)
+
+
+def test_prefill_conv_in_pieces_matches_one_call():
+    """Two calls with the recurrent and conv states carried equal one call bit
+    for bit: the piece boundary is a chunk boundary, and the carried conv
+    state holds exactly the raw tokens the single call reads."""
+    import gated_deltanet_linear_08_gb300 as gdn
+    lens, cut = [300, 700], 256
+    x = make_prefill_inputs(PrefillCase("conv_pieces", seqlens=lens, hk=2, hv=4, init_state=True, gated_norm=True,
+                                        seed=47))
+    cv = make_conv_inputs(conv_channels(2, 4), 4, 2, seed=47)
+    d = to_dev(x)
+    w, st = cv["weight"].cuda(), cv["state"].cuda()
+    kw = dict(z=d["z"], norm_w=d["norm_w"], eps=x["eps"], conv_weight=w)
+    full_out, full_fin, full_cs = gdn.prefill(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"],
+                                              d["cu_seqlens"], init_state=d["init_state"], conv_state=st, **kw)
+    starts = [0, lens[0]]
+    out = torch.empty_like(full_out)
+    states, cstates = d["init_state"], st
+    for lo, hi in ((0, cut), (cut, None)):
+        rows = [torch.arange(s + lo, s + (l if hi is None else hi), device="cuda") for s, l in zip(starts, lens)]
+        sel = torch.cat(rows)
+        cu = torch.tensor([0, len(rows[0]), len(rows[0]) + len(rows[1])], dtype=torch.int32, device="cuda")
+        pick = lambda t: t.index_select(0, sel).contiguous()
+        o, states, cstates = gdn.prefill(pick(d["q"]), pick(d["k"]), pick(d["v"]), pick(d["a"]), pick(d["b"]),
+                                         d["A_log"], d["dt_bias"], cu, init_state=states, conv_state=cstates,
+                                         **dict(kw, z=pick(d["z"])))
+        out.index_copy_(0, sel, o)
+    torch.cuda.synchronize()
+    assert torch.equal(out, full_out) and torch.equal(states, full_fin) and torch.equal(cstates, full_cs)
+    assert gdn.check_device_status() == 0
+
+
+def _decode_conv(case, width):
+    import gated_deltanet_linear_08_gb300 as gdn
+    x = make_decode_slots_inputs(case)
+    B, T, P = case.batch, case.tokens, case.slots
+    cv = make_conv_inputs(conv_channels(case.hk, case.hv), width, P, seed=case.seed)
+    # raw inputs off the conv's rounding ties (live sequences, from their slots)
+    idx_all = x["state_idx"].tolist()
+    X = torch.cat([x[m].reshape(B * T, -1) for m in ("q", "k", "v")], dim=1)
+    states = [cv["state"][i] if 0 <= i < P else None for i in idx_all]
+    conv_nudge_off_ties(X, list(range(0, B * T + 1, T)), cv["weight"], states)
+    q, k, v = split_qkv(X, case.hk, case.hv)
+    x["q"], x["k"], x["v"] = (t.reshape(B, T, *t.shape[1:]) for t in (q, k, v))
+    dev = "cuda"
+    pool = x["pool"].to(dev)
+    cpool = cv["state"].to(dev)
+    out = gdn.decode_slots(*(x[n].to(dev) for n in ("q", "k", "v", "a", "b")), x["A_log"].to(dev),
+                           x["dt_bias"].to(dev), pool, state_idx=x["state_idx"].to(dev),
+                           z=None if x["z"] is None else x["z"].to(dev),
+                           norm_w=None if x["norm_w"] is None else x["norm_w"].to(dev), eps=x["eps"],
+                           conv_weight=cv["weight"].to(dev), conv_state=cpool)
+    bits = gdn.check_device_status()
+    got_out, got_pool, got_cpool = out.double().cpu().numpy(), pool.cpu(), cpool.cpu()
+
+    idx = x["state_idx"].numpy()
+    live = np.nonzero((idx >= 0) & (idx < P))[0]
+    dead = np.nonzero((idx < 0) | (idx >= P))[0]
+    w = to_f64(cv["weight"])
+    cst = to_f64(cv["state"])
+    hk, hv, d = case.hk, case.hv, case.d
+    # the oracle: each live sequence's conv over its draft from its slot's
+    # history, then one decode step per token
+    qc = np.zeros((len(live), T, hk, d)); kc = np.zeros_like(qc); vc = np.zeros((len(live), T, hv, d))
+    new_c = {}
+    for i, n in enumerate(live):
+        raw = np.concatenate([to_f64(x[m])[n].reshape(T, -1) for m in ("q", "k", "v")], axis=1)
+        y, new_c[idx[n]] = oracle.causal_conv_silu(raw, w, cst[idx[n]])
+        qc[i] = y[:, :hk * d].reshape(T, hk, d)
+        kc[i] = y[:, hk * d:2 * hk * d].reshape(T, hk, d)
+        vc[i] = y[:, 2 * hk * d:].reshape(T, hv, d)
+    S = np.ascontiguousarray(to_f64(x["pool"])[idx[live]])
+    ref = np.zeros((len(live), T, hv, d))
+    for t in range(T):
+        ref[:, t] = oracle.decode_step(qc[:, t], kc[:, t], vc[:, t], to_f64(x["a"])[live, t],
+                                       to_f64(x["b"])[live, t], to_f64(x["A_log"]), to_f64(x["dt_bias"]), S,
+                                       z=None if x["z"] is None else to_f64(x["z"])[live, t],
+                                       norm_w=to_f64(x["norm_w"]), eps=x["eps"])
+    assert_out_close(got_out[live], ref, "decode conv out")
+    Sg = got_pool[torch.as_tensor(idx[live].astype(np.int64))].double().numpy()
+    assert np.abs(Sg - S).max() / np.abs(S).max() <= DECODE_STATE_REL
+    assert np.all(got_out[dead] == 0)
+    # conv pool: named slots rolled exactly, every other slot untouched
+    for s, v in new_c.items():
+        assert np.array_equal(got_cpool[s].double().numpy(), v), s
+    untouched = torch.as_tensor(np.setdiff1d(np.arange(P), idx[live]))
+    assert torch.equal(got_cpool[untouched], cv["state"][untouched])
+    assert bits == (4 if case.out_of_pool else 0), bits
+
+
+@pytest.mark.parametrize("tokens", [1, 4])
+def test_decode_conv_slots(tokens):
+    _decode_conv(DecodeSlotsCase(f"conv_dec_T{tokens}", batch=48, tokens=tokens, slots=64, skipped=3,
+                                 gated_norm=True, seed=50 + tokens), 4)
+
+
+@pytest.mark.parametrize("width", [1, 2, 3])
+def test_decode_conv_widths_grouped_heads_out_of_pool(width):
+    _decode_conv(DecodeSlotsCase(f"conv_dec_w{width}", batch=9, tokens=2, slots=12, skipped=1, out_of_pool=2,
+                                 hk=2, hv=6, seed=60 + width), width)
+
+
+def test_prefill_then_decode_with_conv_matches_one_prefill():
+    """Serving order: prefill a prompt (recurrent and conv states out), then
+    decode two tokens from those states.  The decoded outputs match the
+    oracle's prefill over prompt + draft."""
+    import gated_deltanet_linear_08_gb300 as gdn
+    L, T, hk, hv = 133, 2, 2, 4
+    x = make_prefill_inputs(PrefillCase("conv_serve", seqlens=[L + T, L + T], hk=hk, hv=hv, init_state=True,
+                                        gated_norm=True, seed=48))
+    cv = make_conv_inputs(conv_channels(hk, hv), 4, 2, seed=48)
+    _off_ties(x, cv)
+    ro, _, _ = _oracle_prefill_conv(x, cv)
+    d = to_dev(x)
+    w = cv["weight"].cuda()
+    prompt = torch.cat([torch.arange(0, L), torch.arange(L + T, 2 * L + T)]).cuda()
+    draft = torch.cat([torch.arange(L, L + T), torch.arange(2 * L + T, 2 * L + 2 * T)]).cuda()
+    pick = lambda t, r: t.index_select(0, r).contiguous()
+    cu = torch.tensor([0, L, 2 * L], dtype=torch.int32, device="cuda")
+    _, fin, cst = gdn.prefill(*(pick(d[n], prompt) for n in ("q", "k", "v", "a", "b")), d["A_log"], d["dt_bias"],
+                              cu, init_state=d["init_state"], z=pick(d["z"], prompt), norm_w=d["norm_w"],
+                              eps=x["eps"], conv_weight=w, conv_state=cv["state"].cuda())
+    dec = lambda t: pick(t, draft).unflatten(0, (2, T))
+    out = gdn.decode_slots(*(dec(d[n]) for n in ("q", "k", "v", "a", "b")), d["A_log"], d["dt_bias"], fin,
+                           z=dec(d["z"]), norm_w=d["norm_w"], eps=x["eps"], conv_weight=w, conv_state=cst)
+    torch.cuda.synchronize()
+    assert gdn.check_device_status() == 0
+    assert_out_close(out.flatten(0, 1).double().cpu().numpy(), ro[draft.cpu().numpy()], "prefill+decode out")
+
+
+def test_graph_captured_decode_with_conv_matches_eager():
+    import gated_deltanet_linear_08_gb300 as gdn
+    case = DecodeSlotsCase("conv_graph", batch=8, tokens=1, slots=16, skipped=1, hk=2, hv=4, seed=70)
+    x = make_decode_slots_inputs(case)
+    cv = make_conv_inputs(conv_channels(2, 4), 4, 16, seed=70)
+    t = {n: x[n].cuda() for n in ("q", "k", "v", "a", "b")}
+    A_log, dt, idx, w = x["A_log"].cuda(), x["dt_bias"].cuda(), x["state_idx"].cuda(), cv["weight"].cuda()
+    steps = 5
+
+    def loop(pool, cpool, outs, stream=None):
+        for s in range(steps):
+            gdn.decode_slots(t["q"], t["k"], t["v"], t["a"], t["b"], A_log, dt, pool, state_idx=idx, out=outs[s],
+                             stream=stream, conv_weight=w, conv_state=cpool)
+
+    outs_e = [torch.empty(8, 1, 4, 128, dtype=torch.bfloat16, device="cuda") for _ in range(steps)]
+    outs_g = [torch.empty_like(o) for o in outs_e]
+    pool_e, cpool_e = x["pool"].cuda(), cv["state"].cuda()
+    loop(pool_e, cpool_e, outs_e)
+    pool_g, cpool_g = x["pool"].cuda(), cv["state"].cuda()
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        loop(pool_g, cpool_g, outs_g, stream=stream)
+    pool_g.copy_(x["pool"].cuda())
+    cpool_g.copy_(cv["state"].cuda())
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(pool_g, pool_e) and torch.equal(cpool_g, cpool_e)
+    assert all(torch.equal(a, b) for a, b in zip(outs_g, outs_e))
+    assert gdn.check_device_status() == 0

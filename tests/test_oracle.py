@@ -403,3 +403,33 @@ def test_conv_inputs_channel_order_is_q_k_v():
     qc, kc, vc, _ = oracle.conv_inputs(np.array([0, T]), q, k, v, w)
     assert np.all(qc == 0) and np.all(kc == 0)
     assert np.array_equal(vc, oracle.round_bf16(v / (1 + np.exp(-v))))
+
+
+def test_conv_tie_nudging_makes_fp32_and_fp64_roundings_agree():
+    """The parity inputs of the conv are moved off bf16 rounding ties
+    (parity_util.conv_nudge_off_ties).  On such inputs an fp32 evaluation --
+    torch on the CPU: fp32 sums of the exact bf16 products, fp32 SiLU --
+    rounds every output with a bf16 ulp of at least 2^-16 exactly as the
+    fp64 oracle does, and the rest to within one such ulp."""
+    import torch
+    from parity_util import TIE_MIN_ULP, conv_nudge_off_ties
+    from gated_deltanet_linear_08_gb300.inputs import make_conv_inputs
+    g = torch.Generator().manual_seed(3)
+    T, C, K = 96, 512, 4
+    X = torch.randn(T, C, generator=g).to(torch.bfloat16)
+    cv = make_conv_inputs(C, K, 1, seed=3)
+    st = cv["state"][0]
+    nudged = conv_nudge_off_ties(X, [0, T], cv["weight"], [st])
+    assert nudged > 0
+    y64, _ = oracle.causal_conv_silu(X.double().numpy(), cv["weight"].double().numpy(), st.double().numpy())
+    xe = torch.cat([st, X]).float()
+    w = cv["weight"].float()
+    acc = w[:, K - 1] * xe[K - 1:K - 1 + T]
+    for j in range(K - 1):
+        acc = acc + w[:, j] * xe[j:j + T]
+    y32 = (acc * torch.sigmoid(acc)).to(torch.bfloat16).double().numpy()
+    _, e = np.frexp(y64)
+    ulp = np.ldexp(1.0, e - 8)
+    big = ulp >= TIE_MIN_ULP
+    assert np.array_equal(y32[big], y64[big])
+    assert np.all(np.abs(y32 - y64)[~big] <= TIE_MIN_ULP)
