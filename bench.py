@@ -41,7 +41,7 @@ from gated_deltanet_linear_08_gb300.inputs import (CASE_DECODE, CASE_T2048, Deco
 METRIC = "GDN prefill tokens/s & decode GB/s at Hv=32,D=128; % of tensor/HBM roofline"
 PREFILL_FLOP_PER_TOKEN_HEAD = 10 * 64 * 128 + 6 * 128 * 128   # 180,224 (C=64 chunked count)
 N_ROTATE = 8
-KERNEL_SOURCES = ["gdn_api.cu", "gdn_decode.cu", "gdn_prefill_prep.cu", "gdn_prefill_scan.cu",
+KERNEL_SOURCES = ["gdn_api.cu", "gdn_conv.cu", "gdn_decode.cu", "gdn_prefill_prep.cu", "gdn_prefill_scan.cu",
                   "gdn_prefill_out.cu", "common.cuh", "conv.cuh", "tc05.cuh", "kernels.h"]
 
 
@@ -389,28 +389,33 @@ def conv_prefill_region(gdn, pre, stream, calls: int = 30, warmup: int = 3):
     w = cv["weight"].to(sets[0]["q"].device)
     states = [cv["state"].to(w.device) for _ in sets]
     outs = [torch.empty_like(st) for st in states]
+    wss = [gdn.alloc_workspace(1, x["q"].shape[0], 16, x["hv"], w.device, conv=True) for _ in sets]
 
     def call(i):
         s = sets[i % len(sets)]
         gdn.prefill(s["q"], s["k"], s["v"], s["a"], s["b"], shared["A_log"], shared["dt_bias"],
                     shared["cu_seqlens"], init_state=None, z=s["z"], norm_w=shared["norm_w"], eps=x["eps"],
-                    out=s["out"], final_state=s["fin"], workspace=s["ws"], stream=stream, conv_weight=w,
+                    out=s["out"], final_state=s["fin"], workspace=wss[i % len(sets)], stream=stream, conv_weight=w,
                     conv_state=states[i % len(sets)], conv_state_out=outs[i % len(sets)])
     return time_calls(call, calls, warmup, stream)
 
 
-def conv_decode_region(gdn, dec, stream, calls: int = 50, warmup: int = 5):
-    """Batch-256 decode with the width-4 conv: the conv-state pool [256, 3,
-    8192] rolled in place by the follow-up kernel."""
+def conv_decode_region(gdn, dec, stream, in_place: bool, calls: int = 50, warmup: int = 5):
+    """Batch-256 decode with the width-4 conv and conv-state pools [256, 3,
+    8192]: two pools used in turn (the decode kernel writes the new states),
+    or one pool rolled in place by the follow-up kernel."""
     B, hv = dec["q"].shape[0], dec["v"].shape[1]
     cv = make_conv_inputs(conv_channels(16, hv), CONV_WIDTH, B, seed=2)
-    w, cpool = cv["weight"].to(dec["q"].device), cv["state"].to(dec["q"].device)
+    w = cv["weight"].to(dec["q"].device)
+    pools = [cv["state"].to(w.device), cv["state"].to(w.device)]
     tok = {n: dec[n].unsqueeze(1) for n in ("q", "k", "v", "a", "b")}
     out = dec["out"].unsqueeze(1)
 
     def call(i):
+        src = pools[i % 2]
+        dst = src if in_place else pools[(i + 1) % 2]
         gdn.decode_slots(tok["q"], tok["k"], tok["v"], tok["a"], tok["b"], dec["A_log"], dec["dt_bias"],
-                         dec["state"], out=out, stream=stream, conv_weight=w, conv_state=cpool)
+                         dec["state"], out=out, stream=stream, conv_weight=w, conv_state=src, conv_state_out=dst)
     return time_calls(call, calls, warmup, stream)
 
 
@@ -561,7 +566,8 @@ def main():
         "tokens_per_s": world * SLOTS_CASE.batch * SLOTS_CASE.tokens / (sl_ms * 1e-3),
         "hbm_frac": sl_bytes / (sl_ms * 1e-3) / 1e9 / peaks["hbm"]}
     cp_ms = max_over_ranks(conv_prefill_region(gdn, pre, stream), world)
-    cd_ms = max_over_ranks(conv_decode_region(gdn, dec, stream), world)
+    cd_ms = max_over_ranks(conv_decode_region(gdn, dec, stream, in_place=False), world)
+    cdi_ms = max_over_ranks(conv_decode_region(gdn, dec, stream, in_place=True), world)
     conv_state_b = CASE_DECODE.batch * (CONV_WIDTH - 1) * conv_channels(16, hv) * 2
     cd_bytes = dbytes + 2 * conv_state_b
     line["conv"] = {
@@ -570,7 +576,10 @@ def main():
         "prefill_overhead_vs_plain": cp_ms / pre_mean - 1.0,
         "decode_ms_per_call": cd_ms, "decode_gbs": cd_bytes / (cd_ms * 1e-3) / 1e9,
         "decode_hbm_frac": cd_bytes / (cd_ms * 1e-3) / 1e9 / peaks["hbm"],
-        "decode_overhead_vs_plain": cd_ms / dec_mean - 1.0}
+        "decode_overhead_vs_plain": cd_ms / dec_mean - 1.0,
+        "decode_pools": "two conv-state pools used in turn (state_out apart from state_in)",
+        "decode_in_place_ms_per_call": cdi_ms,
+        "decode_in_place_overhead_vs_plain": cdi_ms / dec_mean - 1.0}
     if not args.no_e2e:
         e2e_ms, h2d, d2h = e2e_region(gdn, x, dec_y, dev, max(10, min(args.steps, 200)),
                                       3, stream)

@@ -26,7 +26,7 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED",
                 6: "GDN_ERR_WORKSPACE"}
 EXPORTED = ("gdn_status_string", "gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_decode",
             "gdn_check_device_status", "gdn_prefill_noalloc", "gdn_decode_slots", "gdn_prefill_strided",
-            "gdn_decode_strided", "gdn_prefill_conv", "gdn_decode_conv")
+            "gdn_decode_strided", "gdn_prefill_conv", "gdn_decode_conv", "gdn_prefill_conv_workspace_bytes")
 
 
 class GdnError(RuntimeError):
@@ -88,6 +88,8 @@ def load(path: Optional[str] = None):
             lib.gdn_decode_strided.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Strides), ctypes.c_int32,
                                                ctypes.c_int32, P, P, P, P, P, P, P, P, P, P, P, f32, P, P]
             lib.gdn_decode_strided.restype = ctypes.c_int
+            lib.gdn_prefill_conv_workspace_bytes.argtypes = [ctypes.POINTER(Shape)]
+            lib.gdn_prefill_conv_workspace_bytes.restype = sz
             lib.gdn_prefill_conv.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Strides), ctypes.POINTER(Conv),
                                              P, P, P, P, P, P, P, P, P, P, P, f32, P, P, P, sz, P]
             lib.gdn_prefill_conv.restype = ctypes.c_int
@@ -115,8 +117,11 @@ def make_shape(num_seqs: int, total_tokens: int, hk: int, hv: int, hq: Optional[
     return Shape(num_seqs, total_tokens, hk if hq is None else hq, hk, hv, dk, dv)
 
 
-def workspace_bytes(num_seqs: int, total_tokens: int, hk: int, hv: int) -> int:
+def workspace_bytes(num_seqs: int, total_tokens: int, hk: int, hv: int, conv: bool = False) -> int:
+    """Workspace of gdn_prefill, or with ``conv`` of gdn_prefill_conv."""
     s = make_shape(num_seqs, total_tokens, hk, hv)
+    if conv:
+        return int(load().gdn_prefill_conv_workspace_bytes(ctypes.byref(s)))
     return int(load().gdn_prefill_workspace_bytes(ctypes.byref(s)))
 
 
@@ -174,9 +179,10 @@ def _stream_handle(stream: Optional[torch.cuda.Stream], device) -> int:
     return s.cuda_stream
 
 
-def alloc_workspace(num_seqs: int, total_tokens: int, hk: int, hv: int, device) -> torch.Tensor:
-    """Device workspace for gdn_prefill (torch allocation, 1024-byte aligned)."""
-    n = workspace_bytes(num_seqs, total_tokens, hk, hv)
+def alloc_workspace(num_seqs: int, total_tokens: int, hk: int, hv: int, device, conv: bool = False) -> torch.Tensor:
+    """Device workspace for gdn_prefill (with ``conv``: gdn_prefill_conv);
+    a torch allocation, 1024-byte aligned."""
+    n = workspace_bytes(num_seqs, total_tokens, hk, hv, conv)
     buf = torch.empty(n + 1024, dtype=torch.uint8, device=device)
     off = (-buf.data_ptr()) % 1024
     return buf[off:off + n] if n else buf[:0]
@@ -217,7 +223,7 @@ def prefill(q, k, v, a, b, A_log, dt_bias, cu_seqlens, init_state=None, z=None, 
     if final_state is None:
         final_state = torch.empty(N, hv, 128, 128, dtype=torch.float32, device=dev)
     if workspace is None:
-        workspace = alloc_workspace(N, T, hk, hv, dev)
+        workspace = alloc_workspace(N, T, hk, hv, dev, conv=conv_weight is not None)
     bf, f32 = torch.bfloat16, torch.float32
     shape = make_shape(N, T, hk, hv)
     strides = _strides(dict(q=q, k=k, v=v, z=z, a=a, b=b), 1)
@@ -293,12 +299,14 @@ def decode(q, k, v, a, b, A_log, dt_bias, state, z=None, norm_w=None, eps: float
 
 
 def decode_slots(q, k, v, a, b, A_log, dt_bias, state_pool, state_idx=None, z=None, norm_w=None,
-                 eps: float = 1e-6, out=None, stream=None, conv_weight=None, conv_state=None):
+                 eps: float = 1e-6, out=None, stream=None, conv_weight=None, conv_state=None,
+                 conv_state_out=None):
     """``tokens`` consecutive tokens per sequence through ``gdn_decode_slots``;
     the pool slots named by ``state_idx`` are updated in place.  With
     ``conv_weight`` [C, K] bf16 the causal conv1d + SiLU runs ahead of the
     core (``gdn_decode_conv``) and ``conv_state`` [P, K-1, C] bf16, a pool
-    indexed like ``state_pool``, is rolled in place.
+    indexed like ``state_pool``, is rolled in place -- or, given
+    ``conv_state_out`` (a second pool), written there by the decode kernel.
 
     q, k [B, T, Hk, 128] bf16; v [B, T, Hv, 128] bf16; a, b [B, T, Hv] bf16;
     state_pool [P, Hv, 128, 128] fp32; state_idx [B] int32 (device) or None
@@ -319,7 +327,7 @@ def decode_slots(q, k, v, a, b, A_log, dt_bias, state_pool, state_idx=None, z=No
             _in_ptr(z, "z", dev), _ptr(norm_w, bf, "norm_w", dev), float(eps), _ptr(out, bf, "out", dev),
             _stream_handle(stream, dev))
     if conv_weight is not None:
-        conv = _conv(conv_weight, conv_state, conv_state, dev)
+        conv = _conv(conv_weight, conv_state, conv_state if conv_state_out is None else conv_state_out, dev)
         code = load().gdn_decode_conv(ctypes.byref(shape), None if strides is None else ctypes.byref(strides),
                                       ctypes.byref(conv), int(T), int(state_pool.shape[0]), *ins, *rest)
     elif strides is None:

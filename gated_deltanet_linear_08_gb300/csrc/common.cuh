@@ -45,6 +45,14 @@ __device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8])
         f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
     }
 }
+// Unpack 4 bf16 held in an 8-byte vector.
+__device__ __forceinline__ void unpack4(const uint2 &u, float (&f)[4])
+{
+    f[0] = __uint_as_float(u.x << 16);
+    f[1] = __uint_as_float(u.x & 0xFFFF0000u);
+    f[2] = __uint_as_float(u.y << 16);
+    f[3] = __uint_as_float(u.y & 0xFFFF0000u);
+}
 // Pack two floats into bf16x2 (round to nearest even), lo in the low half.
 __device__ __forceinline__ uint32_t pack2(float lo, float hi)
 {

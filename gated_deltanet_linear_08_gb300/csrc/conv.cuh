@@ -18,15 +18,30 @@ namespace gdn {
 
 constexpr int kMaxConvWidth = 4;
 
-template <int N>
-struct ConvWidth {
-    static constexpr int value = N;
-};
-
 // SiLU in fp32: x sigmoid(x), exact to a few fp32 ulps.
 __device__ __forceinline__ float silu_f(float x) { return __fdividef(x, 1.f + __expf(-x)); }
 
-// First element of the 8 conv channels c .. c+7 (c a multiple of 8) of token
+// Weights of the N channels c .. c+N-1 (c a multiple of 4), w[j][e] for tap
+// j of channel c+e: N*KW contiguous bf16 read as 8-byte vectors (the weight
+// array is 16-byte aligned and a channel group starts at a multiple of 8 B).
+template <int N, int KW>
+__device__ __forceinline__ void conv_weights(const __nv_bfloat16 *weight, int c, float (&w)[KW][N])
+{
+    static_assert((N * KW) % 4 == 0, "whole 8-byte vectors");
+    const uint2 *src = reinterpret_cast<const uint2 *>(weight + (size_t)c * KW);
+#pragma unroll
+    for (int v = 0; v < N * KW / 4; ++v) {
+        const uint2 u = src[v];
+        const uint32_t h[2] = {u.x, u.y};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int f = 4 * v + k;   // flat index e * KW + j
+            w[f % KW][f / KW] = __uint_as_float(k & 1 ? (h[k >> 1] & 0xFFFF0000u) : (h[k >> 1] << 16));
+        }
+    }
+}
+
+// First element of conv channels c, c+1, ... (c a multiple of 4) of token
 // `tok` in the token inputs, which hold each head as 128 contiguous channels.
 __device__ __forceinline__ const __nv_bfloat16 *conv_src(const void *q, const void *k, const void *v,
                                                          const InputStrides &in, int hk, int c, int64_t tok)

@@ -106,7 +106,7 @@ gdn_status_t resolve_conv(const gdn_conv_t *c, const gdn_shape_t *s, size_t rows
     o.weight = static_cast<const __nv_bfloat16 *>(c->weight);
     o.state_in = static_cast<const __nv_bfloat16 *>(c->state_in);
     o.state_out = static_cast<__nv_bfloat16 *>(c->state_out);
-    if (!aligned(c->weight, 2) || !aligned(c->state_in, 16) || !aligned(c->state_out, 16))
+    if (!aligned(c->weight, 16) || !aligned(c->state_in, 16) || !aligned(c->state_out, 16))
         return GDN_ERR_ALIGNMENT;
     state_bytes = rows * (size_t)(c->width - 1) * (size_t)o.channels * 2;
     if (c->state_in != c->state_out && overlaps(c->state_in, state_bytes, c->state_out, state_bytes))
@@ -142,6 +142,14 @@ size_t gdn_prefill_workspace_bytes(const gdn_shape_t *s)
     return gdn::prefill_workspace_bytes(s->num_seqs, s->total_tokens, s->hk, s->hv);
 }
 
+size_t gdn_prefill_conv_workspace_bytes(const gdn_shape_t *s)
+{
+    if (check_shape(s) != GDN_OK || s->total_tokens <= 0)
+        return 0;
+    return gdn::prefill_workspace_bytes(s->num_seqs, s->total_tokens, s->hk, s->hv)
+           + gdn::prefill_conv_bytes(s->total_tokens, s->hk, s->hv);
+}
+
 gdn_status_t gdn_prefill_conv(const gdn_shape_t *s, const gdn_strides_t *strides, const gdn_conv_t *conv,
                               const void *q, const void *k, const void *v, const void *a, const void *b,
                               const float *A_log, const float *dt_bias, const float *init_state,
@@ -171,7 +179,8 @@ gdn_status_t gdn_prefill_conv(const gdn_shape_t *s, const gdn_strides_t *strides
             return GDN_ERR_ALIGNMENT;
     if (!aligned(a, 2) || !aligned(b, 2))   // read one element at a time
         return GDN_ERR_ALIGNMENT;
-    const size_t need = gdn::prefill_workspace_bytes(s->num_seqs, s->total_tokens, s->hk, s->hv);
+    const size_t core_need = gdn::prefill_workspace_bytes(s->num_seqs, s->total_tokens, s->hk, s->hv);
+    const size_t need = core_need + (conv ? gdn::prefill_conv_bytes(s->total_tokens, s->hk, s->hv) : 0);
     if (need > 0 && (!workspace || workspace_bytes < need))
         return GDN_ERR_WORKSPACE;
     if (workspace && !aligned(workspace, 1024))
@@ -213,8 +222,20 @@ gdn_status_t gdn_prefill_conv(const gdn_shape_t *s, const gdn_strides_t *strides
     p.hv = s->hv;
     p.max_chunks = gdn::prefill_max_chunks(s->num_seqs, s->total_tokens);
     p.in = in;
-    p.conv = cv;
     p.q = q; p.k = k; p.v = v; p.a = a; p.b = b;
+    if (conv) {
+        // the conv reads the raw inputs; the core reads its output, q | k | v
+        // rows of `channels` elements in the workspace after the records
+        cv.x_q = q; cv.x_k = k; cv.x_v = v;
+        cv.x_in = in;
+        cv.y = reinterpret_cast<__nv_bfloat16 *>(static_cast<unsigned char *>(workspace) + core_need);
+        const int64_t C = cv.channels;
+        p.q = cv.y;
+        p.k = cv.y + (size_t)s->hk * 128;
+        p.v = cv.y + (size_t)2 * s->hk * 128;
+        p.in.q = {C, 128}; p.in.k = {C, 128}; p.in.v = {C, 128};
+    }
+    p.conv = cv;
     p.A_log = A_log; p.dt_bias = dt_bias;
     p.init_state = init_state;
     p.cu_seqlens = cu_seqlens;

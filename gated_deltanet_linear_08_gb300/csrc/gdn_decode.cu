@@ -74,18 +74,12 @@ decode_kernel(DecodeArgs p)
     if constexpr (KW > 0) {
         if (warp < 3) {
             const int chan = (warp == 0 ? (hk + hq) * kD : warp == 1 ? hq * kD : (2 * hk + h) * kD) + lane * 4;
+            conv_weights<4, KW>(p.conv.weight, chan, cw);
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-#pragma unroll
-                for (int j = 0; j < KW; ++j)
-                    cw[j][e] = bf2f(p.conv.weight[(size_t)(chan + e) * KW + j]);
-#pragma unroll
-            for (int j = 0; j < KW - 1; ++j) {
-                const uint2 u = *reinterpret_cast<const uint2 *>(
-                    p.conv.state_in + (((size_t)slot * (KW - 1) + j) * p.conv.channels + chan));
-                win[j][0] = __uint_as_float(u.x << 16); win[j][1] = __uint_as_float(u.x & 0xFFFF0000u);
-                win[j][2] = __uint_as_float(u.y << 16); win[j][3] = __uint_as_float(u.y & 0xFFFF0000u);
-            }
+            for (int j = 0; j < KW - 1; ++j)
+                unpack4(*reinterpret_cast<const uint2 *>(
+                            p.conv.state_in + (((size_t)slot * (KW - 1) + j) * p.conv.channels + chan)),
+                        win[j]);
         }
     }
     // raw token inputs -> conv + SiLU, rounded to bf16; the window moves on
@@ -117,9 +111,8 @@ decode_kernel(DecodeArgs p)
             const Stride sd = warp == 0 ? p.in.k : p.in.q;
             const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(warp == 0 ? p.k : p.q)
                                        + (int64_t)tok * sd.t + (int64_t)hq * sd.h + lane * 4;
-            const uint2 u = *reinterpret_cast<const uint2 *>(src);
-            float f[4] = {__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
-                          __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u)};
+            float f[4];
+            unpack4(*reinterpret_cast<const uint2 *>(src), f);
             conv4(f);
             float ss = f[0] * f[0] + f[1] * f[1] + f[2] * f[2] + f[3] * f[3];
 #pragma unroll
@@ -133,9 +126,8 @@ decode_kernel(DecodeArgs p)
         } else if (warp == 2) {
             const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(p.v)
                                        + (int64_t)tok * p.in.v.t + (int64_t)h * p.in.v.h + lane * 4;
-            const uint2 u = *reinterpret_cast<const uint2 *>(src);
-            float f[4] = {__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
-                          __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u)};
+            float f[4];
+            unpack4(*reinterpret_cast<const uint2 *>(src), f);
             conv4(f);
 #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -229,12 +221,27 @@ decode_kernel(DecodeArgs p)
 #pragma unroll
     for (int i = 0; i < kRowsPerThread; ++i)
         __stcs(reinterpret_cast<float4 *>(S + (size_t)(warp + kWarps * i) * kD) + lane, st[i]);
+
+    // 7. A separate conv-state pool receives the window now in registers: the
+    //    K-1 last raw inputs of [old state; tokens].  q and k channels come
+    //    from the group's first value head, v channels from every head.  (An
+    //    in-place pool is rolled by the follow-up kernel instead.)
+    if constexpr (KW > 1) {
+        if (warp < 3 && p.conv.state_out && p.conv.state_out != p.conv.state_in
+            && (warp == 2 || h % (hv / hk) == 0)) {
+            const int chan = (warp == 0 ? (hk + hq) * kD : warp == 1 ? hq * kD : (2 * hk + h) * kD) + lane * 4;
+#pragma unroll
+            for (int j = 0; j < KW - 1; ++j)
+                *reinterpret_cast<uint2 *>(p.conv.state_out + (((size_t)slot * (KW - 1) + j) * p.conv.channels + chan))
+                    = make_uint2(pack2(win[j][0], win[j][1]), pack2(win[j][2], win[j][3]));
+        }
+    }
 }
 
-// The conv-state roll after a decode call: one thread per 8 channels of a
-// sequence's slot.  It runs once the decode grid has finished (every value
-// head of a group reads the same q and k history, so none of it may change
-// while any of them still runs).
+// The in-place conv-state roll after a decode call: one thread per 8
+// channels of a sequence's slot.  It runs once the decode grid has finished
+// (every value head of a group reads the same q and k history, so none of it
+// may change while any of them still runs).
 constexpr int kRollThreads = 128;
 
 __global__ void __launch_bounds__(kRollThreads)
@@ -280,7 +287,7 @@ cudaError_t launch_decode(const DecodeArgs &args, cudaStream_t stream)
     else
         launch_width<false>(args, grid, stream);
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || args.conv.width <= 1 || !args.conv.state_out)
+    if (e != cudaSuccess || args.conv.width <= 1 || !args.conv.state_out || args.conv.state_out != args.conv.state_in)
         return e;
     // launched early behind the decode grid; it waits for that grid's end
     cudaLaunchConfig_t cfg = {};

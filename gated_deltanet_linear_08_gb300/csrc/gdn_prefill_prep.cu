@@ -38,7 +38,6 @@
 #include <cuda.h>
 
 #include "common.cuh"
-#include "conv.cuh"
 #include "kernels.h"
 #include "tc05.cuh"
 
@@ -104,7 +103,7 @@ constexpr uint32_t kSmemBytes = kOffSmall + ((sizeof(Small) + 127) / 128) * 128 
 // Locate global chunk `gc`: first token and valid rows.  Returns false when gc
 // lies past the last chunk.  Malformed cu_seqlens (decreasing or outside
 // [0, T]) are treated as empty sequences and flagged.
-__device__ bool locate_chunk(const PrefillArgs &p, int gc, int &tok0, int &L, int &seq, int &seq0, bool &bad)
+__device__ bool locate_chunk(const PrefillArgs &p, int gc, int &tok0, int &L, bool &bad)
 {
     int c = 0;
     bad = false;
@@ -118,8 +117,6 @@ __device__ bool locate_chunk(const PrefillArgs &p, int gc, int &tok0, int &L, in
         if (gc < c + nc) {
             tok0 = s + (gc - c) * kC;
             L = min(kC, e - tok0);
-            seq = n;
-            seq0 = s;
             return true;
         }
         c += nc;
@@ -204,120 +201,6 @@ __device__ void merge_block(unsigned char *sm, const Small *s, int a, int b, int
 
 
 
-// ---- causal conv1d + SiLU on the chunk's k, q and v tiles, in place (the
-// short convolution ahead of the core; the arithmetic is in conv.cuh).
-// Thread t < 192 owns the 16-byte column chunk cc = t % 48 of the 384 tile
-// channels (k, q, v; two 64-channel halves each) over the 16-row run t / 48.
-// Output row i needs raw rows i-K+1 .. i, so each thread first takes the K-1
-// raw rows before its run -- for the first run the tokens before the chunk,
-// or the carried state at a sequence's start -- and only then are the runs
-// rewritten.
-constexpr int kConvThreads = 192;
-constexpr int kConvRun = 16;
-
-// Tile base in shared memory and first conv channel of column chunk cc.
-__device__ __forceinline__ void conv_chunk(const PrefillArgs &p, int cc, int h, int hq, uint32_t &off, int &chan)
-{
-    const int ti = cc >> 3, hf = ti & 1, c8 = (cc & 7) * 8;
-    if (ti < 2) {          // k
-        off = kOffKQ + hf * 16384;
-        chan = (p.hk + hq) * kD + hf * 64 + c8;
-    } else if (ti < 4) {   // q
-        off = kOffQ + hf * 16384;
-        chan = hq * kD + hf * 64 + c8;
-    } else {               // v
-        off = kOffV + hf * 8192;
-        chan = (2 * p.hk + h) * kD + hf * 64 + c8;
-    }
-}
-
-// Weights of this thread's 8 channels, and the raw rows before the first run
-// (issued before the tile copies land).
-template <int KW>
-__device__ __forceinline__ void conv_load(const PrefillArgs &p, int tid, int h, int hq, int seq, int seq0,
-                                          int tok0, float (&w)[KW][8], uint4 (&hist)[kMaxConvWidth - 1])
-{
-    if (tid >= kConvThreads)
-        return;
-    const int cc = tid % 48, run = tid / 48;
-    uint32_t off;
-    int chan;
-    conv_chunk(p, cc, h, hq, off, chan);
-#pragma unroll
-    for (int e = 0; e < 8; ++e)
-#pragma unroll
-        for (int j = 0; j < KW; ++j)
-            w[j][e] = bf2f(p.conv.weight[(size_t)(chan + e) * KW + j]);
-    if (run == 0) {
-#pragma unroll
-        for (int j = 0; j < KW - 1; ++j) {
-            const int pos = tok0 - (KW - 1) + j;
-            hist[j] = make_uint4(0, 0, 0, 0);
-            if (pos >= seq0)
-                hist[j] = *reinterpret_cast<const uint4 *>(conv_src(p.q, p.k, p.v, p.in, p.hk, chan, pos));
-            else if (p.conv.state_in)
-                hist[j] = *reinterpret_cast<const uint4 *>(
-                    p.conv.state_in + (((size_t)seq * (KW - 1) + (KW - 1) + (pos - seq0)) * p.conv.channels + chan));
-        }
-    }
-}
-
-template <int KW>
-__device__ __forceinline__ void conv_apply(const PrefillArgs &p, unsigned char *sm, int tid, int h, int hq,
-                                           const float (&w)[KW][8], uint4 (&hist)[kMaxConvWidth - 1])
-{
-    const int cc = tid % 48, run = tid / 48, c = cc & 7;
-    const bool act = tid < kConvThreads;
-    uint32_t off = 0;
-    int chan;
-    conv_chunk(p, cc, h, hq, off, chan);
-    if (act && run > 0) {
-#pragma unroll
-        for (int j = 0; j < KW - 1; ++j)
-            hist[j] = *reinterpret_cast<const uint4 *>(sm + off + sw128_chunk_offset(run * kConvRun - (KW - 1) + j, c));
-    }
-    __syncthreads();   // every history row is held before any row is rewritten
-    if (act) {
-        float win[KW > 1 ? KW - 1 : 1][8];
-#pragma unroll
-        for (int j = 0; j < KW - 1; ++j)
-            unpack8(hist[j], win[j]);
-#pragma unroll
-        for (int i0 = 0; i0 < kConvRun; i0 += 4) {
-            uint4 raw[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                raw[i] = *reinterpret_cast<const uint4 *>(sm + off + sw128_chunk_offset(run * kConvRun + i0 + i, c));
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float x[8], y[8];
-                unpack8(raw[i], x);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    float acc = w[KW - 1][e] * x[e];
-#pragma unroll
-                    for (int j = 0; j < KW - 1; ++j)
-                        acc = fmaf(w[j][e], win[j][e], acc);
-                    y[e] = silu_f(acc);
-                }
-                *reinterpret_cast<uint4 *>(sm + off + sw128_chunk_offset(run * kConvRun + i0 + i, c)) = pack8(y);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-#pragma unroll
-                    for (int j = 0; j + 1 < KW - 1; ++j)
-                        win[j][e] = win[j + 1][e];
-                    if (KW > 1)
-                        win[KW > 1 ? KW - 2 : 0][e] = x[e];
-                }
-            }
-        }
-    }
-    __syncthreads();
-}
-
-// KW: width of the causal conv ahead of the core (0: none); one instance per
-// width, so the plain path carries no conv code.
-template <int KW>
 __global__ void __launch_bounds__(kThreads, 2)
 prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v)
@@ -329,9 +212,9 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
     const int q = warp & 3, ch = warp >> 2;
     const int row = 32 * q + lane;          // TMEM lane of this thread
 
-    int tok0 = 0, L = 0, seq = 0, seq0 = 0;
+    int tok0 = 0, L = 0;
     bool bad = false;
-    const bool live = locate_chunk(p, gc, tok0, L, seq, seq0, bad);
+    const bool live = locate_chunk(p, gc, tok0, L, bad);
     if (bad && gc == 0 && h == 0 && tid == 0)
         set_status(p.status, kStatusBadSeqlens);
     if (!live)
@@ -364,52 +247,38 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
         tc_fence_before();
     }
     // ---- 2. gates: g, beta, in-chunk inclusive cumsum G (under the copies)
-    auto gates = [&]() {
-        if (tid < 64) {
-            float gv = 0.f, bv = 0.f;
-            if (tid < L) {
-                const int64_t tok = tok0 + tid;
-                gv = gate_f(bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.a)[tok * p.in.a.t + h * p.in.a.h]),
-                            p.A_log[h], p.dt_bias[h]);
-                bv = sigmoid_f(bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.b)[tok * p.in.b.t + h * p.in.b.h]));
-            }
-            float c = gv;
+    if (tid < 64) {
+        float gv = 0.f, bv = 0.f;
+        if (tid < L) {
+            const int64_t tok = tok0 + tid;
+            gv = gate_f(bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.a)[tok * p.in.a.t + h * p.in.a.h]),
+                        p.A_log[h], p.dt_bias[h]);
+            bv = sigmoid_f(bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.b)[tok * p.in.b.t + h * p.in.b.h]));
+        }
+        float c = gv;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float t = __shfl_up_sync(0xffffffffu, c, o);
-                if (lane >= o) c += t;
-            }
-            s->G2[tid] = c;
-            s->beta[tid] = bv;
+        for (int o = 1; o < 32; o <<= 1) {
+            const float t = __shfl_up_sync(0xffffffffu, c, o);
+            if (lane >= o) c += t;
         }
-        __syncthreads();
-        float Gnat = 0.f;
-        if (tid < 64)
-            Gnat = s->G2[tid] + (tid >= 32 ? s->G2[31] : 0.f);
-        __syncthreads();
-        if (tid < 64) {
-            s->G2[tid] = Gnat * kLog2e;
-            s->gam[tid] = expf(Gnat);
-        }
-        __syncthreads();
-        if (tid < 64)
-            s->eps[tid] = (tid < L) ? exp2f(s->G2[63] - s->G2[tid]) : 0.f;
-        if (tid == 0)
-            *reinterpret_cast<float4 *>(ws + kWsScal) = make_float4(exp2f(s->G2[63]), 0.f, 0.f, 0.f);
-    };
-    if constexpr (KW > 0) {
-        // with the conv: its loads go out first, the gates run under them, and
-        // the tiles are convolved in place once they land
-        float w[KW][8];
-        uint4 hist[kMaxConvWidth - 1];
-        conv_load<KW>(p, tid, h, hq, seq, seq0, tok0, w, hist);
-        gates();
-        wait_bar(s, &s->mbar_tma, 0, p.status);
-        conv_apply<KW>(p, sm, tid, h, hq, w, hist);
-    } else {
-        gates();
-        wait_bar(s, &s->mbar_tma, 0, p.status);
+        s->G2[tid] = c;
+        s->beta[tid] = bv;
     }
+    __syncthreads();
+    float Gnat = 0.f;
+    if (tid < 64)
+        Gnat = s->G2[tid] + (tid >= 32 ? s->G2[31] : 0.f);
+    __syncthreads();
+    if (tid < 64) {
+        s->G2[tid] = Gnat * kLog2e;
+        s->gam[tid] = expf(Gnat);
+    }
+    __syncthreads();
+    if (tid < 64)
+        s->eps[tid] = (tid < L) ? exp2f(s->G2[63] - s->G2[tid]) : 0.f;
+    if (tid == 0)
+        *reinterpret_cast<float4 *>(ws + kWsScal) = make_float4(exp2f(s->G2[63]), 0.f, 0.f, 0.f);
+    wait_bar(s, &s->mbar_tma, 0, p.status);
 
     // rows past the chunk's end hold the next sequence's tokens (or the
     // copy's zero fill): clear them in all six tiles
@@ -830,41 +699,24 @@ bool encode_tile_map(CUtensorMap *map, const void *base, int heads, int tokens, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-namespace {
 
-template <int KW>
-cudaError_t launch_width(const PrefillArgs &p, dim3 grid, const CUtensorMap &tq, const CUtensorMap &tk,
-                         const CUtensorMap &tv, cudaStream_t stream)
+cudaError_t launch_prefill_prep(const PrefillArgs &p, cudaStream_t stream)
 {
     static bool configured = false;   // attribute is per function, process-wide
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(prep_kernel<KW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess)
             return e;
         configured = true;
     }
-    prep_kernel<KW><<<grid, kThreads, kSmemBytes, stream>>>(p, tq, tk, tv);
-    return cudaGetLastError();
-}
-
-}  // namespace
-
-cudaError_t launch_prefill_prep(const PrefillArgs &p, cudaStream_t stream)
-{
     CUtensorMap tq, tk, tv;
     if (!encode_tile_map(&tq, p.q, p.hk, p.total_tokens, p.in.q.t, p.in.q.h)
         || !encode_tile_map(&tk, p.k, p.hk, p.total_tokens, p.in.k.t, p.in.k.h)
         || !encode_tile_map(&tv, p.v, p.hv, p.total_tokens, p.in.v.t, p.in.v.h))
         return cudaErrorInvalidValue;
     dim3 grid(p.max_chunks, p.hv);
-    switch (p.conv.width) {
-    case 1: return launch_width<1>(p, grid, tq, tk, tv, stream);
-    case 2: return launch_width<2>(p, grid, tq, tk, tv, stream);
-    case 3: return launch_width<3>(p, grid, tq, tk, tv, stream);
-    case 4: return launch_width<4>(p, grid, tq, tk, tv, stream);
-    default: return launch_width<0>(p, grid, tq, tk, tv, stream);
-    }
+    prep_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p, tq, tk, tv);
+    return cudaGetLastError();
 }
 
 }  // namespace gdn

@@ -230,7 +230,7 @@ scan_kernel(PrefillArgs p)
             if (lane < (h % grp == 0 ? 12 : 4)) {
                 const int part = lane >> 2, c = r * kNv + (lane & 3) * 8;
                 const int chan = part == 0 ? (2 * p.hk + h) * kD + c : part == 1 ? hq * kD + c : (p.hk + hq) * kD + c;
-                conv_roll8(p.conv, p.q, p.k, p.v, p.in, p.hk, chan, n, n, tok0, len);
+                conv_roll8(p.conv, p.conv.x_q, p.conv.x_k, p.conv.x_v, p.conv.x_in, p.hk, chan, n, n, tok0, len);
             }
         }
     } else {

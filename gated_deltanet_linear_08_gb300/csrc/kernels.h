@@ -22,12 +22,17 @@ struct InputStrides {
 
 // Causal conv1d + SiLU over the q | k | v channels ahead of the core
 // (width 0: none).  state_in / state_out: bf16 [rows][width-1][channels].
+// x_q, x_k, x_v / x_in: the raw token inputs the conv reads (and the state
+// roll copies); for prefill the core then reads the conv output y instead.
 struct ConvArgs {
     int width;
     int channels;               // Hk*128 + Hk*128 + Hv*128
     const __nv_bfloat16 *weight;   // [channels][width]
     const __nv_bfloat16 *state_in;
     __nv_bfloat16 *state_out;
+    const void *x_q, *x_k, *x_v;
+    InputStrides x_in;
+    __nv_bfloat16 *y;           // prefill: conv output [tokens][channels]
 };
 
 struct DecodeArgs {
@@ -100,6 +105,14 @@ inline size_t prefill_workspace_bytes(int num_seqs, int total_tokens, int hk, in
     return c * (size_t)hv * kPerVHead;
 }
 
+// With the conv, the prefill workspace also holds its output y, bf16
+// [tokens][channels], after the records.
+inline size_t prefill_conv_bytes(int total_tokens, int hk, int hv)
+{
+    const size_t b = (size_t)(total_tokens > 0 ? total_tokens : 0) * (size_t)(2 * hk + hv) * 128 * 2;
+    return (b + 1023) & ~size_t(1023);
+}
+
 // Tensor map over a bf16 tensor of `tokens` x `heads` rows of 128 elements,
 // `st` elements between tokens and `sh` between heads (multiples of 8): boxes
 // of 64 tokens x 64 elements of one head, 128-byte swizzled in shared memory,
@@ -114,10 +127,18 @@ cudaError_t launch_decode(const DecodeArgs &args, cudaStream_t stream);
 cudaError_t launch_prefill_prep(const PrefillArgs &args, cudaStream_t stream);
 cudaError_t launch_prefill_scan(const PrefillArgs &args, cudaStream_t stream);
 cudaError_t launch_prefill_out(const PrefillArgs &args, cudaStream_t stream);
+// The conv ahead of the prefill core: y = silu(conv(x)) for every token, in
+// stream order before prep (which then reads y through args.q/k/v).
+cudaError_t launch_prefill_conv(const PrefillArgs &args, cudaStream_t stream);
 inline cudaError_t launch_prefill(const PrefillArgs &args, cudaStream_t stream)
 {
     if (args.num_seqs == 0)
         return cudaSuccess;
+    if (args.total_tokens > 0 && args.conv.width > 0) {
+        cudaError_t e = launch_prefill_conv(args, stream);
+        if (e != cudaSuccess)
+            return e;
+    }
     if (args.total_tokens > 0) {
         cudaError_t e = launch_prefill_prep(args, stream);
         if (e != cudaSuccess)

@@ -233,7 +233,7 @@ gdn_status_t gdn_decode_strided(const gdn_shape_t *shape, const gdn_strides_t *s
                                 void *out, void *stream);
 
 /*
- * Causal conv1d + SiLU ahead of the core, fused into it (the JevAny page,
+ * Causal conv1d + SiLU ahead of the core (the JevAny page,
  * "Add opt-in fused Qwen3.5 inference kernels", Measurements, lists
  * causal-conv1d among the path's dependencies; its definition here is a
  * reading).  Over the C = Hk*128 + Hk*128 + Hv*128 channels q | k | v of
@@ -243,7 +243,7 @@ gdn_status_t gdn_decode_strided(const gdn_shape_t *shape, const gdn_strides_t *s
  * sequence's first token come from its carried state: the K-1 raw inputs
  * that preceded it, oldest first.  z is not convolved.
  *   width     1..4
- *   weight    bf16 [C][width], 2-byte aligned
+ *   weight    bf16 [C][width], 16-byte aligned
  *   state_in  bf16 [rows][K-1][C], 16-byte aligned: one row per sequence for
  *             prefill (rows = N; NULL means zeros), the slot pool for decode
  *             (rows = num_slots, sequence n at its slot; required if K > 1)
@@ -264,8 +264,16 @@ typedef struct {
     void *state_out;
 } gdn_conv_t;
 
+/* Bytes of device workspace gdn_prefill_conv needs: gdn_prefill's, plus
+ * room for the conv output (total_tokens x C bf16).  Host-only. */
+size_t gdn_prefill_conv_workspace_bytes(const gdn_shape_t *shape);
+
 /* gdn_prefill_strided with the conv ahead of the core; conv == NULL is
- * gdn_prefill_strided. */
+ * gdn_prefill_strided.  The conv runs as its own pass over all tokens and
+ * writes its output into the workspace, which must hold
+ * gdn_prefill_conv_workspace_bytes (else GDN_ERR_WORKSPACE); the core then
+ * reads it there.  The carried states are rolled once every read of the old
+ * ones has finished, so state_out may be state_in. */
 gdn_status_t gdn_prefill_conv(const gdn_shape_t *shape, const gdn_strides_t *strides,
                               const gdn_conv_t *conv,
                               const void *q, const void *k, const void *v,
@@ -279,9 +287,11 @@ gdn_status_t gdn_prefill_conv(const gdn_shape_t *shape, const gdn_strides_t *str
 
 /* gdn_decode_strided with the conv ahead of the core; conv->state_in is the
  * conv-state pool, indexed like state_pool.  Skipped and out-of-pool
- * sequences leave their conv state untouched.  With conv->state_out set,
- * a second small kernel rolls the states once the decode grid has finished
- * (the heads of a group share their q and k history). */
+ * sequences leave their conv state untouched.  A state_out apart from
+ * state_in (a second pool, e.g. used in turn with the first) is written by
+ * the decode kernel itself; with state_out == state_in a second small kernel
+ * rolls the pool in place once the decode grid has finished (the value
+ * heads of a group share their q and k history). */
 gdn_status_t gdn_decode_conv(const gdn_shape_t *shape, const gdn_strides_t *strides,
                              const gdn_conv_t *conv, int32_t tokens, int32_t num_slots,
                              const void *q, const void *k, const void *v,

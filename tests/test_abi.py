@@ -188,7 +188,7 @@ def test_conv_entry_points_reject_bad_descriptors(lib):
         assert call(width=0) == 1                    # width outside 1..4
         assert call(width=5) == 1
         assert call(weight=None) == 1
-        assert call(weight=W + 1) == 3               # bf16 weights need 2-byte alignment
+        assert call(weight=W + 8) == 3               # weights need 16-byte alignment
         assert call(sin=S + 8, sout=S + 8) == 3      # states need 16-byte alignment
         assert call(sout=S + 4096) == 1              # partial overlap of the two states
         assert call(sout=FAKE + 0x20000000) == 1     # written state over an input (v)

@@ -137,7 +137,7 @@ def test_prefill_conv_in_pieces_matches_one_call():
     assert gdn.check_device_status() == 0
 
 
-def _decode_conv(case, width):
+def _decode_conv(case, width, out_of_place=False):
     import gated_deltanet_linear_08_gb300 as gdn
     x = make_decode_slots_inputs(case)
     B, T, P = case.batch, case.tokens, case.slots
@@ -152,12 +152,20 @@ def _decode_conv(case, width):
     dev = "cuda"
     pool = x["pool"].to(dev)
     cpool = cv["state"].to(dev)
+    cpool_in = cpool
+    if out_of_place:
+        # a second pool receives the rolled states; the first stays as it was
+        fill = torch.full_like(cv["state"], 0.5)
+        cpool = fill.to(dev)
     out = gdn.decode_slots(*(x[n].to(dev) for n in ("q", "k", "v", "a", "b")), x["A_log"].to(dev),
                            x["dt_bias"].to(dev), pool, state_idx=x["state_idx"].to(dev),
                            z=None if x["z"] is None else x["z"].to(dev),
                            norm_w=None if x["norm_w"] is None else x["norm_w"].to(dev), eps=x["eps"],
-                           conv_weight=cv["weight"].to(dev), conv_state=cpool)
+                           conv_weight=cv["weight"].to(dev), conv_state=cpool_in,
+                           conv_state_out=cpool if out_of_place else None)
     bits = gdn.check_device_status()
+    if out_of_place:
+        assert torch.equal(cpool_in.cpu(), cv["state"])
     got_out, got_pool, got_cpool = out.double().cpu().numpy(), pool.cpu(), cpool.cpu()
 
     idx = x["state_idx"].numpy()
@@ -191,7 +199,7 @@ def _decode_conv(case, width):
     for s, v in new_c.items():
         assert np.array_equal(got_cpool[s].double().numpy(), v), s
     untouched = torch.as_tensor(np.setdiff1d(np.arange(P), idx[live]))
-    assert torch.equal(got_cpool[untouched], cv["state"][untouched])
+    assert torch.equal(got_cpool[untouched], (fill if out_of_place else cv["state"])[untouched])
     assert bits == (4 if case.out_of_pool else 0), bits
 
 
@@ -199,6 +207,15 @@ def _decode_conv(case, width):
 def test_decode_conv_slots(tokens):
     _decode_conv(DecodeSlotsCase(f"conv_dec_T{tokens}", batch=48, tokens=tokens, slots=64, skipped=3,
                                  gated_norm=True, seed=50 + tokens), 4)
+
+
+@pytest.mark.parametrize("tokens", [1, 2])
+def test_decode_conv_into_a_second_pool(tokens):
+    # the decode kernel writes the rolled states itself (no follow-up kernel)
+    _decode_conv(DecodeSlotsCase(f"conv_dec_pp_T{tokens}", batch=40, tokens=tokens, slots=64, skipped=2,
+                                 gated_norm=True, seed=56 + tokens), 4, out_of_place=True)
+    _decode_conv(DecodeSlotsCase(f"conv_dec_pp_g3_T{tokens}", batch=9, tokens=tokens, slots=12, skipped=1,
+                                 out_of_pool=1, hk=2, hv=6, seed=58 + tokens), 3, out_of_place=True)
 
 
 @pytest.mark.parametrize("width", [1, 2, 3])
@@ -265,3 +282,50 @@ def test_graph_captured_decode_with_conv_matches_eager():
     assert torch.equal(pool_g, pool_e) and torch.equal(cpool_g, cpool_e)
     assert all(torch.equal(a, b) for a, b in zip(outs_g, outs_e))
     assert gdn.check_device_status() == 0
+
+
+@pytest.mark.parametrize("out_of_place", [False, True])
+def test_decode_conv_writes_nothing_past_the_pools_or_outputs(out_of_place):
+    """Guard rows after the state pool, the conv-state pools and the output
+    stay bit for bit as they were.  The out-of-pool index equals the pool
+    size, so it names exactly the first guard row."""
+    import gated_deltanet_linear_08_gb300 as gdn
+    case = DecodeSlotsCase("conv_guard", batch=9, tokens=2, slots=12, skipped=1, out_of_pool=2, hk=2, hv=6,
+                           seed=71)
+    x = make_decode_slots_inputs(case)
+    B, T, P, G = case.batch, case.tokens, case.slots, 2
+    cv = make_conv_inputs(conv_channels(2, 6), 3, P + G, seed=71)
+    dev = "cuda"
+    pool = torch.cat([x["pool"], torch.full((G, 6, 128, 128), 3.0)]).to(dev)
+    cin = cv["state"].to(dev)
+    cout = torch.full_like(cin, 0.25) if out_of_place else cin
+    out = torch.full((B + G, T, 6, 128), 5.0, dtype=torch.bfloat16, device=dev)
+    guards = (pool[P:].clone(), cin[P:].clone(), cout[P:].clone(), out[B:].clone())
+    gdn.decode_slots(*(x[n].to(dev) for n in ("q", "k", "v", "a", "b")), x["A_log"].to(dev), x["dt_bias"].to(dev),
+                     pool[:P], state_idx=x["state_idx"].to(dev), out=out[:B], conv_weight=cv["weight"].to(dev),
+                     conv_state=cin[:P], conv_state_out=cout[:P] if out_of_place else None)
+    assert gdn.check_device_status() == 4   # the range bit for the out-of-pool indices
+    for g, now in zip(guards, (pool[P:], cin[P:], cout[P:], out[B:])):
+        assert torch.equal(g, now)
+    dead = [i for i, s in enumerate(x["state_idx"].tolist()) if s < 0 or s >= P]
+    assert bool((out[dead] == 0).all())
+
+
+def test_prefill_conv_writes_nothing_past_the_states_or_outputs():
+    import gated_deltanet_linear_08_gb300 as gdn
+    x = make_prefill_inputs(PrefillCase("conv_guard_p", seqlens=[70, 2, 129], hk=2, hv=6, init_state=True,
+                                        gated_norm=True, seed=72))
+    N, T, G = 3, 201, 2
+    cv = make_conv_inputs(conv_channels(2, 6), 4, N + G, seed=72)
+    d = to_dev(x)
+    cs_in = cv["state"].cuda()
+    cs_out = torch.full_like(cs_in, 0.75)
+    out = torch.full((T + G, 6, 128), 5.0, dtype=torch.bfloat16, device="cuda")
+    fin = torch.full((N + G, 6, 128, 128), 9.0, device="cuda")
+    guards = (cs_out[N:].clone(), out[T:].clone(), fin[N:].clone())
+    gdn.prefill(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["cu_seqlens"],
+                init_state=d["init_state"], z=d["z"], norm_w=d["norm_w"], eps=x["eps"], out=out[:T],
+                final_state=fin[:N], conv_weight=cv["weight"].cuda(), conv_state=cs_in[:N], conv_state_out=cs_out[:N])
+    assert gdn.check_device_status() == 0
+    for g, now in zip(guards, (cs_out[N:], out[T:], fin[N:])):
+        assert torch.equal(g, now)
