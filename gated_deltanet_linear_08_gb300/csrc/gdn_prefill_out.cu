@@ -266,7 +266,7 @@ out_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_z, const __grid
             ++k;
         }
         if (tid == 0)
-            bulk_wait_all();
+            bulk_wait_read<0>();   // the tile copies have read shared memory; they complete with the grid
     }
 
     tc_fence_before();

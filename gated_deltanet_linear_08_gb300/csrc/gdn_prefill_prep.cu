@@ -80,6 +80,7 @@ constexpr uint32_t kOffStFc = kOffTb;    // Fc, after MT
 constexpr uint32_t kOffStEc = kOffAh;    // Ec as the fp16 A operand of Bc, after the inverse
 constexpr uint32_t kOffStQc = kOffP;     // Qc, after [W; R]
 constexpr uint32_t kOffStMc = kOffKQ;    // Mc, after Mc
+constexpr uint32_t kOffStBc = kOffAh;    // Bc (over Ec and the V slices), after Bc
 constexpr uint32_t kTmaBytes = 6 * 8192;   // k, q, v: two 64x64 bf16 boxes each
 
 // TMEM: D_a in [0,64), MT in [64,128); then Ec in [0,64) and [W; R] in
@@ -546,36 +547,13 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
     wait_bar(s, &s->mbar_mma, 0, p.status);
     tc_fence_after();
 
-    // ---- 9. rows 0-63 of [W; R] -> BM = -diag(eps) W; rows 64-127 ->
-    //         Qc = diag(Gam r_q) Q - R (q from the tile still in shared
-    //         memory); every lane's Ec row -> workspace.  Columns: dk half ch.
+    // ---- 9. every lane's Ec row -> the fp16 A operand of Bc; rows 0-63 of
+    //         [W; R] -> BM = -diag(eps) W.  Columns: dk half ch.  The Mc and
+    //         Bc products need only these two images (and TMEM free of Ec
+    //         and [W; R]), so they are issued as soon as both are staged; the
+    //         R rows (64-127) become Qc = diag(Gam r_q) Q - R meanwhile.
+    const int i = row & 63;
     {
-        const int i = row & 63;
-        const float ei = s->eps[i];
-        const float qs = (q >= 2) ? s->gam[i] * s->rq[i] : 0.f;
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-            float dv[32];
-            tmem_ld32(s->tmem_base + ((uint32_t)(32 * q) << 16) + 128 + ch * 64 + g * 32, dv);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int c = g * 4 + u;   // 16-byte chunk within the dk half
-                float w8[8];
-                if (q >= 2) {
-                    float qv[8];
-                    unpack8(*reinterpret_cast<const uint4 *>(sm + kOffQ + ch * 16384 + sw128_chunk_offset(i, c)), qv);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        w8[e] = fmaf(qs, qv[e], -dv[u * 8 + e]);
-                    *reinterpret_cast<uint4 *>(sm + kOffStQc + ch * 8192 + sw128_chunk_offset(i, c)) = pack8h(w8);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        w8[e] = -ei * dv[u * 8 + e];
-                    *reinterpret_cast<uint4 *>(sm + kOffBM + ch * 8192 + sw128_chunk_offset(i, c)) = pack8h(w8);
-                }
-            }
-        }
         float ev[32];
         tmem_ld32(s->tmem_base + ((uint32_t)(32 * q) << 16) + ch * 32, ev);
 #pragma unroll
@@ -586,16 +564,36 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
             *reinterpret_cast<uint4 *>(sm + kOffStEc + sw128_chunk_offset(row, ch * 4 + c)) = pack8h(e8);
         }
     }
+    float wr[2][32];
+    tmem_ld32x2(s->tmem_base + ((uint32_t)(32 * q) << 16) + 128 + ch * 64,
+                s->tmem_base + ((uint32_t)(32 * q) << 16) + 128 + ch * 64 + 32, wr[0], wr[1]);
+    if (q < 2) {
+        const float ei = s->eps[i];
+#pragma unroll
+        for (int g = 0; g < 2; ++g)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                float w8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    w8[e] = -ei * wr[g][u * 8 + e];
+                *reinterpret_cast<uint4 *>(sm + kOffBM + ch * 8192 + sw128_chunk_offset(i, g * 4 + u)) = pack8h(w8);
+            }
+    }
+    if (tid == 0)
+        bulk_wait_read<0>();   // the V and Fc copies are done with their staging (Bc goes there)
     fence_async_smem();
     tc_fence_before();
-    __syncthreads();
+    // barrier 1: the W warps (q < 2, warp 0 among them) wait for every thread
+    // to have staged its Ec row and read [W; R]; the R warps only arrive
+    if (q < 2)
+        named_sync(1, kThreads);
+    else
+        named_arrive(1, kThreads);
 
-    if (tid == 0) {
-        bulk_s2g(ws + kWsQc0, sm + kOffStQc, 16384);
-    }
-    // ---- 10. Mc = Kn^T BM into TMEM [0,128) (Ec has been read) and
-    //          Bc = Ec V into [128,256) ([W; R] has been read); A = the fp16
-    //          Ec image, B = the V slices read MN-major (slices 4 KB apart)
+    // ---- 10. Mc = Kn^T BM into TMEM [0,128) and Bc = Ec V into [128,256);
+    //          A = the fp16 Ec image, B = the V slices read MN-major (slices
+    //          4 KB apart)
     if (warp == 0) {
         tc_fence_after();
         if (lane == 0) {
@@ -613,47 +611,93 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
         }
         __syncwarp();
     }
+    // the R warps (q >= 2: warps 2, 3, 6, 7) turn R into Qc under the products
+    // (q from the tile still in shared memory) and copy it out
+    if (q >= 2) {
+        const float qs = s->gam[i] * s->rq[i];
+#pragma unroll
+        for (int g = 0; g < 2; ++g)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int c = g * 4 + u;   // 16-byte chunk within the dk half
+                float qv[8], w8[8];
+                unpack8(*reinterpret_cast<const uint4 *>(sm + kOffQ + ch * 16384 + sw128_chunk_offset(i, c)), qv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    w8[e] = fmaf(qs, qv[e], -wr[g][u * 8 + e]);
+                *reinterpret_cast<uint4 *>(sm + kOffStQc + ch * 8192 + sw128_chunk_offset(i, c)) = pack8h(w8);
+            }
+        // this warp's 32 Qc rows of dk half ch are 4 KB of the image: out now
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            const uint32_t off = ch * 8192 + (q - 2) * 4096;
+            bulk_s2g(ws + kWsQc0 + off, sm + kOffStQc + off, 4096);
+        }
+    }
     wait_bar(s, &s->mbar_mma, 1, p.status);
     tc_fence_after();
     // Mc row = lane (output dk), columns = input dk half ch
+    {
+        float mv[2][32];
+        tmem_ld32x2(s->tmem_base + ((uint32_t)(32 * q) << 16) + ch * 64,
+                    s->tmem_base + ((uint32_t)(32 * q) << 16) + ch * 64 + 32, mv[0], mv[1]);
 #pragma unroll
-    for (int g = 0; g < 2; ++g) {
-        float mv[32];
-        tmem_ld32(s->tmem_base + ((uint32_t)(32 * q) << 16) + ch * 64 + g * 32, mv);
+        for (int g = 0; g < 2; ++g)
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            float m8[8];
+            for (int u = 0; u < 4; ++u) {
+                float m8[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) m8[e] = mv[u * 8 + e];
-            *reinterpret_cast<uint4 *>(sm + kOffStMc + ch * 16384 + sw128_chunk_offset(row, g * 4 + u)) = pack8h(m8);
+                for (int e = 0; e < 8; ++e) m8[e] = mv[g][u * 8 + e];
+                *reinterpret_cast<uint4 *>(sm + kOffStMc + ch * 16384 + sw128_chunk_offset(row, g * 4 + u)) = pack8h(m8);
+            }
+        // this warp's 32 rows of dk half ch: 4 KB of the Mc image
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            const uint32_t off = ch * 16384 + q * 4096;
+            bulk_s2g(ws + kWsMc0 + off, sm + kOffStMc + off, 4096);
         }
     }
 
     // Bc row = lane (dk), value columns 64 ch .. = slices 2 ch, 2 ch + 1, in
-    // 64-byte-swizzled rows: each thread writes one 64-byte row per slice, a
-    // warp 2 KB
+    // 64-byte-swizzled rows, staged over Ec and the V slices (both read by
+    // the finished products) for one bulk copy
+    {
+        float bv[2][32];
+        tmem_ld32x2(s->tmem_base + ((uint32_t)(32 * q) << 16) + 128 + ch * 64,
+                    s->tmem_base + ((uint32_t)(32 * q) << 16) + 128 + ch * 64 + 32, bv[0], bv[1]);
 #pragma unroll
-    for (int g = 0; g < 2; ++g) {
-        float bv[32];
-        tmem_ld32(s->tmem_base + ((uint32_t)(32 * q) << 16) + 128 + ch * 64 + g * 32, bv);
-        unsigned char *dst = ws + kWsBc + (2 * ch + g) * 8192;
+        for (int g = 0; g < 2; ++g) {
+            unsigned char *dst = sm + kOffStBc + (2 * ch + g) * 8192;   // the record's byte image
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            float b8[8];
+            for (int u = 0; u < 4; ++u) {
+                float b8[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) b8[e] = bv[u * 8 + e];
-            *reinterpret_cast<uint4 *>(dst + sw64_chunk_offset(row, u)) = pack8h(b8);
+                for (int e = 0; e < 8; ++e) b8[e] = bv[g][u * 8 + e];
+                *reinterpret_cast<uint4 *>(dst + sw64_chunk_offset(row, u)) = pack8h(b8);
+            }
+        }
+        // this warp's 32 rows of slices 2 ch and 2 ch + 1: 2 KB of each
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                const uint32_t off = (2 * ch + g) * 8192 + q * 2048;
+                bulk_s2g(ws + kWsBc + off, sm + kOffStBc + off, 2048);
+            }
         }
     }
 
-    // ---- teardown: Mc out, and every staged copy complete before the CTA exits
-    fence_async_smem();
+    // ---- teardown: every staged copy has read its shared memory before the
+    //      CTA exits (each issuing lane waits for its own copies; the writes
+    //      complete with the grid, before the dependent kernels'
+    //      griddepcontrol.wait returns)
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) {
-        bulk_s2g(ws + kWsMc0, sm + kOffStMc, 32768);
-        bulk_wait_all();
-    }
+    if (lane == 0)
+        bulk_wait_read<0>();
     grid_dep_launch();   // the scan kernel may start launching
     if (warp == 0) {
         tc_fence_after();

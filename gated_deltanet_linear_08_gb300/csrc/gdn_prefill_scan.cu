@@ -192,7 +192,7 @@ scan_kernel(PrefillArgs p)
             __syncwarp();
         }
         if (lane == 0)
-            bulk_wait_all();   // every S copy complete before exit
+            bulk_wait_read<0>();   // every S copy has read shared memory; the writes complete with the grid
         __syncwarp();
     } else if (warp == kLoaderWarp) {
         // ------------------------------------------------------------ loader
