@@ -14,14 +14,24 @@
 // row.
 //
 // A persistent grid (one CTA per SM) walks the units with a two-stage
-// pipeline, so the copies for the next unit overlap this unit's products and
-// epilogue:
-//   warp 2      loads a unit's [Qc | Fc | V | S] run and its z tile
-//   warp 3      issues the 12 MMAs into one of two TMEM accumulators
-//   warps 0, 1, 4, 5, 8, 9, 12, 13
-//               epilogue (TMEM lanes 0-63 are readable by warps w with
-//               w % 4 < 2): scale, gated RMSNorm, bf16 tile, tensor-map store
-//   the other warps idle
+// pipeline, so the copies for the next units overlap this unit's products and
+// epilogue.  TMEM lanes 32q .. 32q+31 are readable only by warps w with
+// w % 4 == q, so a unit's 64 output rows would reach only half of the SM's
+// schedulers; units therefore alternate between lane halves: the odd ones
+// read their A operand 64 rows (8 KB) earlier in shared memory, which puts
+// their rows in lanes 64-127 of the second accumulator, and two epilogue
+// groups run side by side:
+//   warps w % 4 in {0, 1}   epilogue of the even units (lanes 0-63)
+//   warps w % 4 in {2, 3}   epilogue of the odd units (lanes 64-127)
+//     each: token row 32 (w % 2) + lane, value columns 32 (w / 4) .. + 31;
+//     scale, gated RMSNorm, bf16 output tile, tensor-map store
+//   warp 16   lane 0 loads a unit's [Qc | Fc | V | S] run into its stage once
+//             the products of the unit two before are done with it; lane 1
+//             loads its z tile once the epilogue two units before has read
+//             that stage's tile; lane 2 issues the 12 MMAs into the unit's
+//             accumulator
+// The run (72 KB) is released by the products and the z tile (16 KB) by the
+// epilogue, so the next-but-one unit's run is in flight during an epilogue.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc05.cuh"
@@ -29,8 +39,9 @@
 namespace gdn {
 namespace {
 
-constexpr int kThreads = 16 * 32;
-constexpr int kLoaderWarp = 2, kIssuerWarp = 3;
+constexpr int kEpiWarps = 16;
+constexpr int kRoleWarp = kEpiWarps;            // lanes 0, 1, 2: loader, z loader, issuer
+constexpr int kThreads = (kEpiWarps + 1) * 32;
 // Stage: the record's [Qc | Fc | V | S] run (72 KB) as copied, then the unit's
 // 64 x 128 bf16 tile of z (tensor-map copy, dk halves of 8 KB, 128-byte
 // swizzle), which the epilogue overwrites with the outputs.
@@ -39,16 +50,22 @@ constexpr uint32_t kRunBytes = 73728;
 constexpr uint32_t kOffY = kRunBytes;
 constexpr uint32_t kStageBytes = kRunBytes + 16384;
 constexpr int kStages = 2;
-constexpr uint32_t kOffSmall = kStages * kStageBytes;
+// Two output tiles of 64 x 128 bf16 (dk halves of 8 KB, 128-byte swizzle),
+// used in turn: a unit's stage is released as soon as its z tile and
+// accumulator are read, and its output tile only has to be read by the
+// tensor-map store before the unit after next writes it again.
+constexpr uint32_t kOffOut = kStages * kStageBytes;
+constexpr uint32_t kOffSmall = kOffOut + 2 * 16384;
 constexpr uint32_t kTmemCols = 256;          // two 128-column accumulators
-constexpr uint32_t kBarEpi = 1, kCntEpi = 256;   // the eight epilogue warps
+constexpr uint32_t kBarEpi = 1, kCntEpi = 256;   // barrier 1 + g: the eight warps of epilogue group g
 constexpr float kScale = 0.088388347648318440550f;  // 1/sqrt(128)
 
 struct Small {
-    float red[4][64];          // row sums of squares of each 32-column quarter
-    uint64_t full[kStages];    // run and z tile landed
-    uint64_t mfull[kStages];   // accumulator written
-    uint64_t efree[kStages];   // epilogue done: tile stored, accumulator read
+    float red[2][4][64];       // per epilogue group: row sums of squares of each 32-column quarter
+    uint64_t full[kStages];    // record run landed
+    uint64_t zfull[kStages];   // z tile landed
+    uint64_t mfull[kStages];   // accumulator written (the record run is free again)
+    uint64_t efree[kStages];   // epilogue done: accumulator and z tile read
     uint32_t tmem_base;
     int fail;
 };
@@ -100,6 +117,7 @@ out_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_z, const __grid
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&s->full[i], 1);
+            mbar_init(&s->zfull[i], 1);
             mbar_init(&s->mfull[i], 1);
             mbar_init(&s->efree[i], 1);
         }
@@ -120,9 +138,9 @@ out_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_z, const __grid
     // grid) and counts only the live ones, so stage k % 2 and barrier phases
     // agree across roles.
 
-    if (warp == kLoaderWarp) {
-        // ------------------------------------------------------------ loader
+    if (warp == kRoleWarp) {
         if (lane == 0) {
+            // -------------------------------------------------------- loader
             int k = 0, issued[kStages] = {0, 0};
             for (int u = blockIdx.x; u < units; u += gridDim.x) {
                 const int gc = u / hv, h = u - gc * hv;
@@ -130,19 +148,15 @@ out_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_z, const __grid
                 if (!locate_chunk(p, gc, tok0, L))
                     continue;
                 const int st = k & 1;
-                // the unit two before used this stage: its tile must be stored
-                if (k >= kStages && !wait_bar(s, &s->efree[st], ((uint32_t)(k >> 1) & 1) ^ 1, p.status))
+                // the unit two before used this stage's run: its products must be done
+                if (k >= kStages && !wait_bar(s, &s->mfull[st], ((uint32_t)(k >> 1) & 1) ^ 1, p.status))
                     break;
                 unsigned char *stage = sm + st * kStageBytes;
                 const unsigned char *rec = p.workspace + ((size_t)gc * hv + h) * kPerVHead;
-                mbar_arrive_expect_tx(&s->full[st], kRunBytes + (kNorm ? 16384u : 0u));
+                mbar_arrive_expect_tx(&s->full[st], kRunBytes);
 #pragma unroll
                 for (int j = 0; j < 3; ++j)
                     bulk_g2s(stage + j * 24576, rec + kWsQc0 + j * 24576, 24576, &s->full[st]);
-                if (kNorm) {
-                    tma_load_3d(stage + kOffY, &tm_z, 0, h, tok0, &s->full[st]);
-                    tma_load_3d(stage + kOffY + 8192, &tm_z, 64, h, tok0, &s->full[st]);
-                }
                 ++issued[st];
                 ++k;
             }
@@ -152,11 +166,32 @@ out_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_z, const __grid
                     if (issued[i] > 0)
                         mbar_wait(&s->full[i], (uint32_t)(issued[i] - 1) & 1);
             }
-        }
-        __syncwarp();
-    } else if (warp == kIssuerWarp) {
-        // ------------------------------------------------------------ issuer
-        if (lane == 0) {
+        } else if (lane == 1 && kNorm) {
+            // ------------------------------------------------------ z loader
+            int k = 0, issued[kStages] = {0, 0};
+            for (int u = blockIdx.x; u < units; u += gridDim.x) {
+                const int gc = u / hv, h = u - gc * hv;
+                int tok0 = 0, L = 0;
+                if (!locate_chunk(p, gc, tok0, L))
+                    continue;
+                const int st = k & 1;
+                // the unit two before read this stage's z tile in its epilogue
+                if (k >= kStages && !wait_bar(s, &s->efree[st], ((uint32_t)(k >> 1) & 1) ^ 1, p.status))
+                    break;
+                unsigned char *stage = sm + st * kStageBytes;
+                mbar_arrive_expect_tx(&s->zfull[st], 16384u);
+                tma_load_3d(stage + kOffY, &tm_z, 0, h, tok0, &s->zfull[st]);
+                tma_load_3d(stage + kOffY + 8192, &tm_z, 64, h, tok0, &s->zfull[st]);
+                ++issued[st];
+                ++k;
+            }
+            if (*reinterpret_cast<volatile int *>(&s->fail)) {
+                for (int i = 0; i < kStages; ++i)
+                    if (issued[i] > 0)
+                        mbar_wait(&s->zfull[i], (uint32_t)(issued[i] - 1) & 1);
+            }
+        } else if (lane == 2) {
+            // -------------------------------------------------------- issuer
             constexpr uint32_t idesc = make_idesc_f16(128, 128, false, true);
             int k = 0;
             for (int u = blockIdx.x; u < units; u += gridDim.x) {
@@ -164,14 +199,18 @@ out_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_z, const __grid
                 if (!locate_chunk(p, u / hv, tok0, L))
                     continue;
                 const int st = k & 1;
-                const uint32_t stg = sbase + st * kStageBytes, d = tbase + st * 128;
+                // odd units: A starts 64 rows (8 KB) early, so the unit's rows
+                // are rows 64-127 (the rows before are whatever precedes them
+                // in shared memory, and their accumulator lanes are not read)
+                const uint32_t stg = sbase + st * kStageBytes - (st ? 8192u : 0u), d = tbase + st * 128;
+                const uint32_t stb = sbase + st * kStageBytes;
                 bool ok = wait_bar(s, &s->full[st], (uint32_t)(k >> 1) & 1, p.status);
                 if (ok && k >= kStages)   // accumulator st read by the epilogue two units ago
                     ok = wait_bar(s, &s->efree[st], ((uint32_t)(k >> 1) & 1) ^ 1, p.status);
                 if (ok) {
                     tc_fence_after();
-                    const uint64_t bv = make_desc(stg + kOffV, 4096, 512, kSw64);
-                    const uint64_t bs = make_desc(stg + kOffS, 8192, 512, kSw64);
+                    const uint64_t bv = make_desc(stb + kOffV, 4096, 512, kSw64);
+                    const uint64_t bs = make_desc(stb + kOffS, 8192, 512, kSw64);
                     const uint64_t af = make_desc(stg + kOffFc, 16, 1024, kSw128);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)   // Fc V over the chunk's 64 tokens
@@ -187,11 +226,12 @@ out_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_z, const __grid
             }
         }
         __syncwarp();
-    } else if ((warp & 3) < 2) {
+    } else {
         // ------------------------------------------------------------ epilogue
-        // token row 32 (w % 4) + lane, value columns 32 (w / 4) .. + 31
-        const int q = warp & 3, cq = warp >> 2;
-        const int row = 32 * q + lane;
+        const int qd = warp & 3, g = qd >> 1, cq = warp >> 2;   // lane quadrant, group, column quarter
+        const int row = 32 * (qd & 1) + lane;                    // token row of the unit
+        const bool lead = lane == 0 && warp == 2 * g;            // the group's store thread
+        const uint32_t bar = kBarEpi + g;
         int k = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x) {
             const int gc = u / hv, h = u - gc * hv;
@@ -199,24 +239,34 @@ out_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_z, const __grid
             if (!locate_chunk(p, gc, tok0, L))
                 continue;
             const int st = k & 1;
+            ++k;
+            if (st != g)
+                continue;
             // this thread's 32 columns: 16-byte chunks 4 (cq & 1) .. of dk half cq / 2
             unsigned char *yt = sm + st * kStageBytes + kOffY + (cq >> 1) * 8192;
+            unsigned char *ot = sm + kOffOut + g * 16384 + (cq >> 1) * 8192;
             const int c0 = (cq & 1) * 4;
-            wait_bar(s, &s->full[st], (uint32_t)(k >> 1) & 1, p.status);      // z tile visible
-            wait_bar(s, &s->mfull[st], (uint32_t)(k >> 1) & 1, p.status);
+            const uint32_t ph = (uint32_t)((k - 1) >> 1) & 1;
+            // the group's output tile was last stored two units ago: that
+            // store must have read it before the tile is written again
+            if (lead)
+                bulk_wait_read<0>();
+            if (kNorm)
+                wait_bar(s, &s->zfull[st], ph, p.status);   // z tile visible
+            wait_bar(s, &s->mfull[st], ph, p.status);
             tc_fence_after();
             float o[32];
-            tmem_ld32(tbase + st * 128 + ((uint32_t)(32 * q) << 16) + cq * 32, o);
+            tmem_ld32(tbase + st * 128 + ((uint32_t)(32 * qd) << 16) + cq * 32, o);
 #pragma unroll
             for (int j = 0; j < 32; ++j) o[j] *= kScale;
             if (kNorm) {
                 float ss = 0.f;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) ss = fmaf(o[j], o[j], ss);
-                s->red[cq][row] = ss;
-                named_sync(kBarEpi, kCntEpi);
-                const float rn = rsqrtf((s->red[0][row] + s->red[1][row] + s->red[2][row] + s->red[3][row])
-                                        * (1.f / kD) + p.eps);
+                s->red[g][cq][row] = ss;
+                named_sync(bar, kCntEpi);
+                const float rn = rsqrtf((s->red[g][0][row] + s->red[g][1][row] + s->red[g][2][row]
+                                         + s->red[g][3][row]) * (1.f / kD) + p.eps);
                 const __nv_bfloat16 *wg = reinterpret_cast<const __nv_bfloat16 *>(p.norm_w) + cq * 32;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -227,6 +277,8 @@ out_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_z, const __grid
                     for (int e = 0; e < 8; ++e)   // silu(z) = z / (1 + e^-z)
                         o[8 * j + e] = o[8 * j + e] * rn * wf[e] * __fdividef(zf[e], 1.f + __expf(-zf[e]));
                 }
+            } else {
+                named_sync(bar, kCntEpi);   // the lead's wait for the output tile
             }
             if (L == kC) {
                 // whole chunk: bf16 outputs into the tile, one tensor-map store per dk half
@@ -235,7 +287,7 @@ out_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_z, const __grid
                     float v[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) v[e] = o[8 * j + e];
-                    *reinterpret_cast<uint4 *>(yt + sw128_chunk_offset(row, c0 + j)) = pack8(v);
+                    *reinterpret_cast<uint4 *>(ot + sw128_chunk_offset(row, c0 + j)) = pack8(v);
                 }
                 fence_async_smem();
             } else if (row < L) {
@@ -252,20 +304,18 @@ out_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_z, const __grid
                 }
             }
             tc_fence_before();
-            named_sync(kBarEpi, kCntEpi);   // accumulator read, tile complete, red consumed
-            if (tid == 0) {
+            named_sync(bar, kCntEpi);   // accumulator and z read, tile complete, red consumed
+            if (lead) {
+                mbar_arrive(&s->efree[st]);   // the stage's z tile and the accumulator are free
                 if (L == kC) {
-                    unsigned char *tile = sm + st * kStageBytes + kOffY;
+                    unsigned char *tile = sm + kOffOut + g * 16384;
                     tma_store_3d(&tm_o, 0, h, tok0, tile);
                     tma_store_3d(&tm_o, 64, h, tok0, tile + 8192);
                     bulk_commit();
-                    bulk_wait_read<0>();
                 }
-                mbar_arrive(&s->efree[st]);
             }
-            ++k;
         }
-        if (tid == 0)
+        if (lead)
             bulk_wait_read<0>();   // the tile copies have read shared memory; they complete with the grid
     }
 
