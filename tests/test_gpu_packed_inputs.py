@@ -70,3 +70,40 @@ def test_decode_reads_inputs_from_a_packed_projection():
     torch.cuda.synchronize()
     assert torch.equal(got, ref) and torch.equal(pool, pool_ref)
     assert gdn.check_device_status() == 0
+
+
+def test_conv_reads_inputs_from_a_packed_projection():
+    """The serving order: one packed projection row per token, the causal conv
+    over its q | k | v blocks, then the core.  Equal bit for bit to the same
+    calls on dense copies, for prefill and for a slot-pool decode step."""
+    import gated_deltanet_linear_08_gb300 as gdn
+    from gated_deltanet_linear_08_gb300.inputs import conv_channels, make_conv_inputs
+    x = make_prefill_inputs(PrefillCase("packed_conv", seqlens=[130, 2, 64], hk=2, hv=4, init_state=True,
+                                        gated_norm=True, seed=33))
+    d = to_dev(x)
+    cv = make_conv_inputs(conv_channels(2, 4), 4, 3, seed=33)
+    w, cs = cv["weight"].cuda(), cv["state"].cuda()
+    common = dict(init_state=d["init_state"], norm_w=d["norm_w"], eps=x["eps"], conv_weight=w, conv_state=cs)
+    ref = gdn.prefill(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["cu_seqlens"],
+                      z=d["z"], **common)
+    buf, q, k, v, z, b, a = _pack(d["q"], d["k"], d["v"], d["z"], d["b"], d["a"])
+    got = gdn.prefill(q, k, v, a, b, d["A_log"], d["dt_bias"], d["cu_seqlens"], z=z, **common)
+    torch.cuda.synchronize()
+    assert all(torch.equal(g, r) for g, r in zip(got, ref))
+
+    y = make_decode_slots_inputs(DecodeSlotsCase("packed_conv_dec", batch=6, tokens=2, slots=8, skipped=1,
+                                                 hk=2, hv=4, gated_norm=True, seed=34))
+    t = {n: y[n].cuda() for n in ("q", "k", "v", "a", "b", "z")}
+    A_log, dt, idx, nw = y["A_log"].cuda(), y["dt_bias"].cuda(), y["state_idx"].cuda(), y["norm_w"].cuda()
+    cvd = make_conv_inputs(conv_channels(2, 4), 4, 8, seed=34)
+    wd = cvd["weight"].cuda()
+    pool_r, pool_g = y["pool"].cuda(), y["pool"].cuda()
+    cp_r, cp_g = cvd["state"].cuda(), cvd["state"].cuda()
+    o_r = gdn.decode_slots(t["q"], t["k"], t["v"], t["a"], t["b"], A_log, dt, pool_r, state_idx=idx, z=t["z"],
+                           norm_w=nw, conv_weight=wd, conv_state=cp_r)
+    buf2, q2, k2, v2, z2, b2, a2 = _pack(t["q"], t["k"], t["v"], t["z"], t["b"], t["a"])
+    o_g = gdn.decode_slots(q2, k2, v2, a2, b2, A_log, dt, pool_g, state_idx=idx, z=z2, norm_w=nw,
+                           conv_weight=wd, conv_state=cp_g)
+    torch.cuda.synchronize()
+    assert torch.equal(o_g, o_r) and torch.equal(pool_g, pool_r) and torch.equal(cp_g, cp_r)
+    assert gdn.check_device_status() == 0
