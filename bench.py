@@ -407,7 +407,7 @@ CONV_WIDTH = 4
 
 
 def conv_prefill_region(gdn, pre, stream, calls: int = 30, warmup: int = 3):
-    """The T = 2048 prefill with the width-4 causal conv + SiLU fused ahead of
+    """The T = 2048 prefill with the width-4 causal conv + SiLU ahead of
     the core (weights [8192, 4], a carried conv state in and out)."""
     x, shared, sets = pre
     C = conv_channels(16, x["hv"])

@@ -24,7 +24,9 @@
  *     owns every buffer and the stream; the library never allocates, frees,
  *     prints, aborts or traps, and issues no host<->device synchronisation in
  *     gdn_prefill / gdn_decode.
- *   - Layouts are row-major, innermost index last, densely packed.
+ *   - Layouts are row-major, innermost index last, densely packed (the
+ *     *_strided and *_conv entry points also take token inputs as strided
+ *     views, see gdn_strides_t).
  *   - bf16 tensors and fp32 state/workspace pointers must be 16-byte aligned
  *     (GDN_ERR_ALIGNMENT otherwise), except a and b (2-byte, read element by
  *     element); the workspace must be 1024-byte aligned.
@@ -301,10 +303,17 @@ gdn_status_t gdn_decode_conv(const gdn_shape_t *shape, const gdn_strides_t *stri
                              const void *z, const void *norm_w, float eps,
                              void *out, void *stream);
 
-/* Reads and clears the device status word that kernels set when a bounded
- * wait runs out.  Synchronises the device: not for the hot path.  Returns
- * GDN_OK, GDN_ERR_DEVICE_STATUS (and the raw bits in *bits when non-NULL),
- * or GDN_ERR_CUDA. */
+/* Reads and clears the device status word the kernels set.  Bits:
+ *   1  a bounded wait on an mbarrier ran out (the kernel skipped the rest of
+ *      its waits and exited; its results are not valid)
+ *   2  malformed cu_seqlens (decreasing, or outside [0, total_tokens]): the
+ *      sequence was treated as empty
+ *   4  a value outside the fp16 operand range (|x| > 65504) met the prefill's
+ *      tensor-core path, or a decode state index was past the pool (that
+ *      sequence was skipped)
+ * Synchronises the device: not for the hot path.  Returns GDN_OK,
+ * GDN_ERR_DEVICE_STATUS (and the raw bits in *bits when non-NULL), or
+ * GDN_ERR_CUDA. */
 gdn_status_t gdn_check_device_status(uint32_t *bits);
 
 #ifdef __cplusplus
