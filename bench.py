@@ -42,7 +42,7 @@ METRIC = "GDN prefill tokens/s & decode GB/s at Hv=32,D=128; % of tensor/HBM roo
 PREFILL_FLOP_PER_TOKEN_HEAD = 10 * 64 * 128 + 6 * 128 * 128   # 180,224 (C=64 chunked count)
 N_ROTATE = 8
 KERNEL_SOURCES = ["gdn_api.cu", "gdn_conv.cu", "gdn_decode.cu", "gdn_prefill_prep.cu", "gdn_prefill_scan.cu",
-                  "gdn_prefill_out.cu", "common.cuh", "conv.cuh", "tc05.cuh", "kernels.h"]
+                  "gdn_prefill_out.cu", "chunks.cuh", "common.cuh", "conv.cuh", "tc05.cuh", "kernels.h"]
 
 
 def load_peaks():

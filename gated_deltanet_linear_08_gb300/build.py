@@ -19,7 +19,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libgdn.so")
 SOURCES = ["gdn_api.cu", "gdn_conv.cu", "gdn_decode.cu", "gdn_prefill_prep.cu", "gdn_prefill_scan.cu",
            "gdn_prefill_out.cu", "gdn_noalloc.cu"]
-HEADERS = ["common.cuh", "conv.cuh", "tc05.cuh", "kernels.h"]
+HEADERS = ["chunks.cuh", "common.cuh", "conv.cuh", "tc05.cuh", "kernels.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "-I", os.path.join(ROOT, "include")]

@@ -86,17 +86,4 @@ __device__ __forceinline__ void set_status(uint32_t *status, uint32_t bits)
         atomicOr(status, bits);
 }
 
-// Chunk bookkeeping for packed sequences: sequence n owns
-// ceil(len_n / 64) chunks, numbered consecutively in sequence order.
-// Returns the number of chunks before sequence n (cu in global memory).
-__device__ __forceinline__ int chunks_before(const int32_t *cu, int n)
-{
-    int c = 0;
-    for (int m = 0; m < n; ++m) {
-        int len = cu[m + 1] - cu[m];
-        c += (len + kC - 1) / kC;
-    }
-    return c;
-}
-
 }  // namespace gdn

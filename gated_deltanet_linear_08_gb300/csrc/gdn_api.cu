@@ -239,6 +239,9 @@ gdn_status_t gdn_prefill_conv(const gdn_shape_t *s, const gdn_strides_t *strides
     p.A_log = A_log; p.dt_bias = dt_bias;
     p.init_state = init_state;
     p.cu_seqlens = cu_seqlens;
+    if (s->num_seqs >= gdn::kIndexMinSeqs && T > 0)
+        p.chunk_off = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(workspace)
+                                                  + gdn::prefill_index_offset(s->num_seqs, s->total_tokens, s->hv));
     p.z = z; p.norm_w = norm_w; p.eps = eps;
     p.out = out;
     p.final_state = final_state;

@@ -32,6 +32,7 @@
 //             accumulator
 // The run (72 KB) is released by the products and the z tile (16 KB) by the
 // epilogue, so the next-but-one unit's run is in flight during an epilogue.
+#include "chunks.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "tc05.cuh"
@@ -71,22 +72,12 @@ struct Small {
 };
 constexpr uint32_t kSmemBytes = kOffSmall + ((sizeof(Small) + 127) / 128) * 128 + 1024;
 
-__device__ bool locate_chunk(const PrefillArgs &p, int gc, int &tok0, int &L)
+// Global chunk gc of the packed sequences: first token and valid rows.
+__device__ __forceinline__ bool locate_chunk(const PrefillArgs &p, int gc, int &tok0, int &L)
 {
-    int c = 0;
-    for (int n = 0; n < p.num_seqs; ++n) {
-        const int s = p.cu_seqlens[n], e = p.cu_seqlens[n + 1];
-        if (s < 0 || e < s || e > p.total_tokens)
-            continue;
-        const int nc = (e - s + kC - 1) / kC;
-        if (gc < c + nc) {
-            tok0 = s + (gc - c) * kC;
-            L = min(kC, e - tok0);
-            return true;
-        }
-        c += nc;
-    }
-    return false;
+    int n;
+    bool bad;
+    return find_chunk(p, gc, n, tok0, L, bad);
 }
 
 __device__ __forceinline__ bool wait_bar(Small *s, uint64_t *bar, uint32_t parity, uint32_t *status)

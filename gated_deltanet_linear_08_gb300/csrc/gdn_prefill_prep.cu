@@ -37,6 +37,7 @@
 // product reads, so no thread waits on a global load.
 #include <cuda.h>
 
+#include "chunks.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "tc05.cuh"
@@ -100,30 +101,6 @@ struct Small {
     int fail;
 };
 constexpr uint32_t kSmemBytes = kOffSmall + ((sizeof(Small) + 127) / 128) * 128 + 1024;
-
-// Locate global chunk `gc`: first token and valid rows.  Returns false when gc
-// lies past the last chunk.  Malformed cu_seqlens (decreasing or outside
-// [0, T]) are treated as empty sequences and flagged.
-__device__ bool locate_chunk(const PrefillArgs &p, int gc, int &tok0, int &L, bool &bad)
-{
-    int c = 0;
-    bad = false;
-    for (int n = 0; n < p.num_seqs; ++n) {
-        int s = p.cu_seqlens[n], e = p.cu_seqlens[n + 1];
-        if (s < 0 || e < s || e > p.total_tokens) {
-            bad = true;
-            continue;
-        }
-        const int nc = (e - s + kC - 1) / kC;
-        if (gc < c + nc) {
-            tok0 = s + (gc - c) * kC;
-            L = min(kC, e - tok0);
-            return true;
-        }
-        c += nc;
-    }
-    return false;
-}
 
 // Bounded wait on one of the CTA's barriers; a timeout is recorded once and
 // later waits are skipped so the CTA runs to its end without hanging.
@@ -213,9 +190,9 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
     const int q = warp & 3, ch = warp >> 2;
     const int row = 32 * q + lane;          // TMEM lane of this thread
 
-    int tok0 = 0, L = 0;
+    int seq = 0, tok0 = 0, L = 0;
     bool bad = false;
-    const bool live = locate_chunk(p, gc, tok0, L, bad);
+    const bool live = find_chunk(p, gc, seq, tok0, L, bad);
     if (bad && gc == 0 && h == 0 && tid == 0)
         set_status(p.status, kStatusBadSeqlens);
     if (!live)
@@ -743,6 +720,74 @@ bool encode_tile_map(CUtensorMap *map, const void *base, int heads, int tokens, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+
+namespace {
+
+// The chunk index: chunk_off[n] = chunks before sequence n (n = 0..N), by one
+// CTA: tiles of 1024 sequences, a block-wide exclusive scan of their chunk
+// counts, and a running carry.  Malformed sequences count no chunks and set
+// the status bit.
+constexpr int kIndexThreads = 1024;
+
+__global__ void __launch_bounds__(kIndexThreads)
+chunk_index_kernel(PrefillArgs p, int32_t *off)
+{
+    __shared__ int wsum[kIndexThreads / 32];
+    __shared__ int carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0)
+        carry = 0;
+    bool bad = false;
+    __syncthreads();
+    for (int base = 0; base < p.num_seqs; base += kIndexThreads) {
+        const int n = base + tid;
+        int nc = 0;
+        if (n < p.num_seqs) {
+            const int s = p.cu_seqlens[n], e = p.cu_seqlens[n + 1];
+            if (seq_ok(p, s, e))
+                nc = (e - s + kC - 1) / kC;
+            else
+                bad = true;
+        }
+        int v = nc;   // inclusive scan within the warp
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += t;
+        }
+        if (lane == 31)
+            wsum[warp] = v;
+        __syncthreads();
+        if (warp == 0) {   // inclusive scan of the warp totals
+            int w = wsum[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += t;
+            }
+            wsum[lane] = w;
+        }
+        __syncthreads();
+        if (n < p.num_seqs)
+            off[n] = carry + (warp ? wsum[warp - 1] : 0) + v - nc;
+        __syncthreads();
+        if (tid == 0)
+            carry += wsum[kIndexThreads / 32 - 1];
+        __syncthreads();
+    }
+    if (tid == 0)
+        off[p.num_seqs] = carry;
+    if (bad)
+        set_status(p.status, kStatusBadSeqlens);
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_index(const PrefillArgs &p, cudaStream_t stream)
+{
+    chunk_index_kernel<<<1, kIndexThreads, 0, stream>>>(p, const_cast<int32_t *>(p.chunk_off));
+    return cudaGetLastError();
+}
 
 cudaError_t launch_prefill_prep(const PrefillArgs &p, cudaStream_t stream)
 {

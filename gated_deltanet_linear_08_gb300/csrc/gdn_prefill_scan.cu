@@ -25,6 +25,7 @@
 //   warp 9      issues the stage copies (four stages: Mc, this CTA's Bc
 //               slice, e^{G_last}), then rolls this CTA's share of the
 //               carried conv state
+#include "chunks.cuh"
 #include "common.cuh"
 #include "conv.cuh"
 #include "kernels.h"
@@ -92,27 +93,6 @@ __device__ __forceinline__ bool wait_quick(Small *s, uint64_t *bar, uint32_t par
     return wait_bar(s, bar, parity, status);
 }
 
-// Chunks that precede sequence n, with the same treatment of malformed
-// cu_seqlens as the prep kernel (a malformed sequence owns no chunks).
-__device__ int chunk_base_of(const PrefillArgs &p, int n, int &tok0, int &len)
-{
-    int c = 0;
-    for (int m = 0; m < p.num_seqs; ++m) {
-        const int s = p.cu_seqlens[m], e = p.cu_seqlens[m + 1];
-        const bool ok = !(s < 0 || e < s || e > p.total_tokens);
-        if (m == n) {
-            tok0 = ok ? s : 0;
-            len = ok ? e - s : 0;
-            return c;
-        }
-        if (ok)
-            c += (e - s + kC - 1) / kC;
-    }
-    tok0 = 0;
-    len = 0;
-    return c;
-}
-
 // Descriptors of the stage operands (shared-memory byte address `st`).
 __device__ __forceinline__ uint64_t desc_k128(uint32_t addr) { return make_desc(addr, 16, 1024, kSw128); }
 
@@ -139,7 +119,9 @@ scan_kernel(PrefillArgs p)
     const uint32_t sbase = smem_u32(sm);
 
     int tok0 = 0, len = 0;
-    const int cbase = chunk_base_of(p, n, tok0, len);
+    const int cbase = chunks_before(p, n, tok0, len);
+    if (r == 0 && h == 0 && tid == 0 && !seq_ok(p, p.cu_seqlens[n], p.cu_seqlens[n + 1]))
+        set_status(p.status, kStatusBadSeqlens);   // treated as empty: final state = initial state
     const int nck = (len + kC - 1) / kC;
     auto record = [&](int c) { return p.workspace + ((size_t)(cbase + c) * hv + h) * kPerVHead; };
 

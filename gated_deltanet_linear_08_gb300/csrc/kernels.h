@@ -60,6 +60,7 @@ struct PrefillArgs {
     const float *A_log, *dt_bias;
     const float *init_state;
     const int32_t *cu_seqlens;
+    const int32_t *chunk_off;      // [N+1] chunks before sequence n, or null (walk cu_seqlens)
     const void *z, *norm_w;
     float eps;
     void *out;
@@ -96,13 +97,23 @@ inline int prefill_max_chunks(int num_seqs, int total_tokens)
 {
     return (total_tokens + 63) / 64 + num_seqs;
 }
+// From this many sequences on, a one-CTA kernel builds the chunk index
+// (chunks before each sequence) ahead of prep; below it, walking cu_seqlens
+// is cheaper than the launch.
+constexpr int kIndexMinSeqs = 16;
+// The workspace: the records, then the chunk index (int32 [N+1], 1 KB
+// aligned), then (with the conv) the conv output.
+inline size_t prefill_index_offset(int num_seqs, int total_tokens, int hv)
+{
+    return (size_t)prefill_max_chunks(num_seqs, total_tokens) * (size_t)hv * kPerVHead;
+}
 inline size_t prefill_workspace_bytes(int num_seqs, int total_tokens, int hk, int hv)
 {
     (void)hk;
     if (total_tokens <= 0)
         return 0;
-    const size_t c = (size_t)prefill_max_chunks(num_seqs, total_tokens);
-    return c * (size_t)hv * kPerVHead;
+    const size_t idx = ((size_t)(num_seqs + 1) * 4 + 1023) & ~size_t(1023);
+    return prefill_index_offset(num_seqs, total_tokens, hv) + idx;
 }
 
 // With the conv, the prefill workspace also holds its output y, bf16
@@ -130,10 +141,17 @@ cudaError_t launch_prefill_out(const PrefillArgs &args, cudaStream_t stream);
 // The conv ahead of the prefill core: y = silu(conv(x)) for every token, in
 // stream order before prep (which then reads y through args.q/k/v).
 cudaError_t launch_prefill_conv(const PrefillArgs &args, cudaStream_t stream);
+// The chunk index args.chunk_off (when set), built before the other kernels.
+cudaError_t launch_chunk_index(const PrefillArgs &args, cudaStream_t stream);
 inline cudaError_t launch_prefill(const PrefillArgs &args, cudaStream_t stream)
 {
     if (args.num_seqs == 0)
         return cudaSuccess;
+    if (args.chunk_off) {
+        cudaError_t e = launch_chunk_index(args, stream);
+        if (e != cudaSuccess)
+            return e;
+    }
     if (args.total_tokens > 0 && args.conv.width > 0) {
         cudaError_t e = launch_prefill_conv(args, stream);
         if (e != cudaSuccess)

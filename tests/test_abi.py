@@ -45,9 +45,11 @@ def test_status_strings(lib):
 
 
 def test_workspace_bytes_formula(lib):
-    # per (chunk, v head) 65 KiB, per (chunk, k head) 16 KiB; chunks <= ceil(T/64) + N
-    assert B.workspace_bytes(1, 2048, 16, 32) == (32 + 1) * 32 * 140288
-    assert B.workspace_bytes(8, 1024, 16, 32) == (16 + 8) * 32 * 140288
+    # one 137 KiB record per (chunk, v head), chunks <= ceil(T/64) + N, then the
+    # chunk index (int32 [N+1], 1 KiB aligned)
+    assert B.workspace_bytes(1, 2048, 16, 32) == (32 + 1) * 32 * 140288 + 1024
+    assert B.workspace_bytes(8, 1024, 16, 32) == (16 + 8) * 32 * 140288 + 1024
+    assert B.workspace_bytes(300, 1024, 16, 32) == (16 + 300) * 32 * 140288 + 2048
     assert B.workspace_bytes(3, 0, 16, 32) == 0
     s = B.make_shape(1, 64, 16, 32, dk=64)
     assert lib.gdn_prefill_workspace_bytes(ctypes.byref(s)) == 0   # unsupported -> 0

@@ -113,3 +113,60 @@ def test_prefill_deterministic_and_stream():
     with torch.cuda.stream(st):
         o2, s2 = gpu_prefill(x, stream=st)
     assert np.array_equal(o1, o2) and np.array_equal(s1, s2)
+
+
+def test_prefill_many_sequences_use_the_chunk_index():
+    """40 packed sequences (empty, single-token, boundary and multi-chunk
+    lengths): from 16 sequences on, the kernels find their chunks through the
+    chunk index instead of walking cu_seqlens."""
+    lens = [0, 1, 63, 64, 65, 130, 2, 0, 200, 17] * 4
+    _check(PrefillCase("many40", seqlens=lens, hk=2, hv=4, init_state=True, gated_norm=True, seed=12))
+
+
+def test_prefill_index_path_equals_walk_path():
+    """24 sequences in one call (chunk index) equal the same sequences in two
+    calls of 12 (walking cu_seqlens), bit for bit."""
+    import gated_deltanet_linear_08_gb300 as gdn
+    lens = [70, 1, 0, 64, 129, 5, 300, 2, 63, 65, 0, 40] * 2
+    x = make_prefill_inputs(PrefillCase("idxwalk", seqlens=lens, hk=2, hv=4, init_state=True, gated_norm=True,
+                                        seed=13))
+    from parity_util import to_dev
+    d = to_dev(x)
+    kw = dict(z=d["z"], norm_w=d["norm_w"], eps=x["eps"])
+    out, fin = gdn.prefill(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["cu_seqlens"],
+                           init_state=d["init_state"], **kw)
+    cu = x["cu_seqlens"].tolist()
+    half = cu[12]
+    for lo, hi, tl, th in ((0, 12, 0, half), (12, 24, half, cu[24])):
+        sl = slice(tl, th)
+        cu_h = torch.tensor([c - tl for c in cu[lo:hi + 1]], dtype=torch.int32, device="cuda")
+        o, f = gdn.prefill(d["q"][sl].contiguous(), d["k"][sl].contiguous(), d["v"][sl].contiguous(),
+                           d["a"][sl].contiguous(), d["b"][sl].contiguous(), d["A_log"], d["dt_bias"], cu_h,
+                           init_state=d["init_state"][lo:hi].contiguous(), z=d["z"][sl].contiguous(),
+                           norm_w=d["norm_w"], eps=x["eps"])
+        torch.cuda.synchronize()
+        assert torch.equal(o, out[sl]) and torch.equal(f, fin[lo:hi])
+    assert gdn.check_device_status() == 0
+
+
+@pytest.mark.parametrize("nseq", [3, 20])
+def test_prefill_malformed_seqlens_are_flagged_and_skipped(nseq):
+    """A sequence whose end lies past the packed tokens is treated as empty
+    (its final state is its initial state) and sets the status bit; the others
+    are computed as usual.  Both the walk (3 sequences) and the chunk index
+    (20) are covered."""
+    import gated_deltanet_linear_08_gb300 as gdn
+    lens = [64, 70, 9, 130][: nseq - 1] if nseq < 5 else ([64, 70, 9, 130] * 5)[: nseq - 1]
+    x = make_prefill_inputs(PrefillCase(f"bad{nseq}", seqlens=lens, hk=2, hv=4, init_state=True, seed=14))
+    T = x["q"].shape[0]
+    from parity_util import to_dev
+    d = to_dev(x)
+    N = len(lens) + 1
+    cu = torch.tensor(x["cu_seqlens"].tolist() + [T + 7], dtype=torch.int32, device="cuda")   # past the end
+    init = torch.cat([d["init_state"], torch.full((1, 4, 128, 128), 0.25, device="cuda")])
+    out, fin = gdn.prefill(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], cu, init_state=init)
+    assert gdn.check_device_status() == 2
+    ro, rs = oracle_prefill(x)
+    assert_out_close(out.double().cpu().numpy(), ro, f"bad{nseq} out")
+    assert_state_close(fin[:N - 1].double().cpu().numpy(), rs, f"bad{nseq} state")
+    assert torch.equal(fin[N - 1], init[N - 1])
