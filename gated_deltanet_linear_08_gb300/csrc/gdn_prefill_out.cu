@@ -245,6 +245,7 @@ out_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_z, const __grid
             if (kNorm)
                 wait_bar(s, &s->zfull[st], ph, p.status);   // z tile visible
             wait_bar(s, &s->mfull[st], ph, p.status);
+            __syncwarp();   // converged (after the lead's wait) for the .aligned TMEM load
             tc_fence_after();
             float o[32];
             tmem_ld32(tbase + st * 128 + ((uint32_t)(32 * qd) << 16) + cq * 32, o);
@@ -280,7 +281,6 @@ out_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_z, const __grid
                     for (int e = 0; e < 8; ++e) v[e] = o[8 * j + e];
                     *reinterpret_cast<uint4 *>(ot + sw128_chunk_offset(row, c0 + j)) = pack8(v);
                 }
-                fence_async_smem();
             } else if (row < L) {
                 // a sequence's ragged last chunk: the rows past it belong to the
                 // next sequence, so each valid row is stored on its own
@@ -294,6 +294,10 @@ out_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_z, const __grid
                     dst[j] = pack8(v);
                 }
             }
+            // one proxy fence for both directions: the output tile's generic
+            // writes before the tensor-map store reads it, and the generic
+            // reads of the z tile before the z loader's TMA refills it
+            fence_async_smem();
             tc_fence_before();
             named_sync(bar, kCntEpi);   // accumulator and z read, tile complete, red consumed
             if (lead) {
@@ -307,7 +311,7 @@ out_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_z, const __grid
             }
         }
         if (lead)
-            bulk_wait_read<0>();   // the tile copies have read shared memory; they complete with the grid
+            bulk_wait_all();   // every output tile copy complete before exit
     }
 
     tc_fence_before();

@@ -348,6 +348,7 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
     __syncthreads();   // the v tile is consumed before [I; P] overwrites it
     if (tid == 0)
         bulk_s2g(ws + kWsV, sm + kOffStV, (uint32_t)kVBytes);
+    __syncwarp();   // warp 0 whole again before the .aligned TMEM loads
 
     // ---- 4. A (fp16 blocks below the diagonal, fp32 diagonal blocks) from
     //         lanes 0-63 and P (fp16, rows 64-127 of [I; P]) from lanes
@@ -501,6 +502,7 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
 
     if (tid == 0)
         bulk_s2g(ws + kWsFc, sm + kOffStFc, 8192);
+    __syncwarp();
     // ---- 8. Ec = Kn^T BE (TMEM [0,64); A = Kn read MN-major: dk halves 16 KB
     //         apart, 16-token steps of 2 KB) and [W; R] = A' Kn (TMEM
     //         [128,256); B = Kn read MN-major)
@@ -559,6 +561,7 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
     }
     if (tid == 0)
         bulk_wait_read<0>();   // the V and Fc copies are done with their staging (Bc goes there)
+    __syncwarp();
     fence_async_smem();
     tc_fence_before();
     // barrier 1: the W warps (q < 2, warp 0 among them) wait for every thread
@@ -667,14 +670,15 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
         }
     }
 
-    // ---- teardown: every staged copy has read its shared memory before the
-    //      CTA exits (each issuing lane waits for its own copies; the writes
-    //      complete with the grid, before the dependent kernels'
-    //      griddepcontrol.wait returns)
+    // ---- teardown: every record copy has completed before the CTA exits (each
+    //      issuing lane waits for its own).  Waiting only for the copies to
+    //      have read shared memory is not enough: a dependent kernel read
+    //      stale records that way.
     tc_fence_before();
     __syncthreads();
     if (lane == 0)
-        bulk_wait_read<0>();
+        bulk_wait_all();
+    __syncwarp();        // warp 0 whole again for the .aligned dealloc
     grid_dep_launch();   // the scan kernel may start launching
     if (warp == 0) {
         tc_fence_after();

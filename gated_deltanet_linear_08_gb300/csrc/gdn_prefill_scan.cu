@@ -22,9 +22,9 @@
 //   warps 0-7   state: warp w holds TMEM lane quadrant w % 4 = state rows
 //               32 (w % 4) .. +31 and value columns 16 (w / 4) .. +15
 //   warp 8      issues every MMA and the copy of S to the workspace
-//   warp 9      issues the stage copies (four stages: Mc, this CTA's Bc
-//               slice, e^{G_last}), then rolls this CTA's share of the
-//               carried conv state
+//   warp 9      issues the stage copies (four stages, or two for short
+//               sequences: Mc, this CTA's Bc slice, e^{G_last}), then
+//               rolls this CTA's share of the carried conv state
 #include "chunks.cuh"
 #include "common.cuh"
 #include "conv.cuh"
@@ -50,26 +50,33 @@ constexpr int kCols = 16;               // value columns per thread
 // and e^{G_last}.
 constexpr uint32_t kStBc = 32768, kStScal = 40960;
 constexpr uint32_t kStageBytes = 41984;
-constexpr int kStages = 4;
 constexpr uint32_t kLoadBytes = 32768 + 8192 + 16;
-
-constexpr uint32_t kOffS = kStages * kStageBytes;   // two S operands [dk][32] fp16, MN-major, 8 KB each
-constexpr uint32_t kOffSmall = kOffS + 16384;
 
 // TMEM columns: chain accumulators at 0 / 32.
 constexpr uint32_t kTmemCols = 64;
 
-struct Small {
-    uint64_t full[kStages];     // stage landed (one arrival + bytes)
-    uint64_t sfree[kStages];    // stage read: the MMAs (one commit) and the eight state warps
+// NS stages of copies ahead of the chain: four (one CTA per SM) hide the
+// copies behind long sequences; two (two CTAs per SM) suit batches of short
+// ones, where each CTA has few chunks and its start-up latency dominates.
+template <int NS>
+struct SmallT {
+    uint64_t full[NS];          // stage landed (one arrival + bytes)
+    uint64_t sfree[NS];         // stage read: the MMAs (one commit) and the eight state warps
     uint64_t bar_chain;
     uint32_t tmem_base;
     int fail;
 };
-constexpr uint32_t kSmemBytes = kOffSmall + ((sizeof(Small) + 127) / 128) * 128 + 1024;
+template <int NS>
+struct ScanCfg {
+    static constexpr uint32_t kOffS = NS * kStageBytes;   // two S operands [dk][32] fp16, MN-major, 8 KB each
+    static constexpr uint32_t kOffSmall = kOffS + 16384;
+    static constexpr uint32_t kSmemBytes = kOffSmall + ((sizeof(SmallT<NS>) + 127) / 128) * 128 + 1024;
+};
 
+template <class Small>
 __device__ __forceinline__ bool failed(Small *s) { return *reinterpret_cast<volatile int *>(&s->fail) != 0; }
 
+template <class Small>
 __device__ __forceinline__ bool wait_bar(Small *s, uint64_t *bar, uint32_t parity, uint32_t *status)
 {
     if (failed(s))
@@ -85,6 +92,7 @@ __device__ __forceinline__ bool wait_bar(Small *s, uint64_t *bar, uint32_t parit
 // Wait that first tests without suspending: a phase that has already
 // completed costs one test.  Spins a little before suspending, for waits on
 // the state chain where the wake-up delay would add to every chunk.
+template <class Small>
 __device__ __forceinline__ bool wait_quick(Small *s, uint64_t *bar, uint32_t parity, uint32_t *status, int spins)
 {
     for (int i = 0; i < spins; ++i)
@@ -105,9 +113,13 @@ __device__ __forceinline__ void issue_mcs(uint32_t d, uint32_t st, uint64_t ds, 
         mma_f16(d, (kk < 4 ? a0 : a1) + (uint64_t)((kk & 3) * 2), ds + (uint64_t)(kk * 64), idesc, kk != 0);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <int NS>
+__global__ void __launch_bounds__(kThreads, NS >= 4 ? 1 : 2)
 scan_kernel(PrefillArgs p)
 {
+    constexpr int kStages = NS;
+    constexpr uint32_t kOffS = ScanCfg<NS>::kOffS, kOffSmall = ScanCfg<NS>::kOffSmall;
+    using Small = SmallT<NS>;
     const int r = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int hv = p.hv;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -174,11 +186,11 @@ scan_kernel(PrefillArgs p)
             __syncwarp();
         }
         if (lane == 0)
-            bulk_wait_read<0>();   // every S copy has read shared memory; the writes complete with the grid
+            bulk_wait_all();   // every S copy complete before exit (the output kernel reads them)
         __syncwarp();
     } else if (warp == kLoaderWarp) {
         // ------------------------------------------------------------ loader
-        int issued[kStages] = {0, 0, 0, 0};
+        int issued[kStages] = {};
         if (lane == 0) {
             for (int c = 0; c < nck; ++c) {
                 const int st = c % kStages;
@@ -256,6 +268,7 @@ scan_kernel(PrefillArgs p)
             const unsigned char *stage = sm + st * kStageBytes;
             wait_quick(s, &s->full[st], (uint32_t)(c / kStages) & 1, p.status, 1);   // Bc, e^{G_last} visible
             wait_quick(s, &s->bar_chain, (uint32_t)c & 1, p.status, 256);
+            __syncwarp();   // converged for the .aligned TMEM load
             tc_fence_after();
             float dv[kCols];
             tmem_ld16(tlane + (c & 1) * kNv, dv);
@@ -263,9 +276,16 @@ scan_kernel(PrefillArgs p)
             uint4 bc[2];
             bc[0] = *reinterpret_cast<const uint4 *>(stage + kStBc + sw64_chunk_offset(row, 2 * cg));
             bc[1] = *reinterpret_cast<const uint4 *>(stage + kStBc + sw64_chunk_offset(row, 2 * cg + 1));
+            // The loader refills this stage by TMA (the async proxy) once it is
+            // free: the generic reads of Bc and e^{G_last} above are ordered
+            // before that write only by a proxy fence, not by the mbarrier.
+            // Without it, with two CTAs per SM, a refill now and then landed
+            // under these reads and S(c+1) took chunk c+2's Bc.
+            fence_async_smem();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&s->sfree[st]);
+            __syncwarp();   // whole warp again before the barrier in put_state
             const __half2 *hp = reinterpret_cast<const __half2 *>(bc);
 #pragma unroll
             for (int j = 0; j < kCols / 2; ++j) {
@@ -294,11 +314,15 @@ scan_kernel(PrefillArgs p)
 
 }  // namespace
 
-cudaError_t launch_prefill_scan(const PrefillArgs &p, cudaStream_t stream)
+namespace {
+
+template <int NS>
+cudaError_t launch_stages(const PrefillArgs &p, cudaStream_t stream)
 {
-    static bool configured = false;
+    static bool configured = false;   // the attribute is per function, process-wide
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(scan_kernel<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)ScanCfg<NS>::kSmemBytes);
         if (e != cudaSuccess)
             return e;
         configured = true;
@@ -306,14 +330,23 @@ cudaError_t launch_prefill_scan(const PrefillArgs &p, cudaStream_t stream)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kTiles, p.hv, p.num_seqs);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = ScanCfg<NS>::kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, scan_kernel, p);
+    return cudaLaunchKernelEx(&cfg, scan_kernel<NS>, p);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_scan(const PrefillArgs &p, cudaStream_t stream)
+{
+    // sequences of two chunks or fewer on average: the lighter two-stage form
+    const bool short_seqs = (int64_t)p.total_tokens <= (int64_t)p.num_seqs * 2 * kC;
+    return short_seqs ? launch_stages<2>(p, stream) : launch_stages<4>(p, stream);
 }
 
 }  // namespace gdn

@@ -319,13 +319,16 @@ __device__ __forceinline__ uint32_t cluster_ctarank()
     return r;
 }
 // Named CTA barriers: producers arrive without waiting, the consumer syncs.
+// The non-.aligned forms, which do not require the warp to arrive converged
+// (the .aligned bar.arrive / bar.sync leave a split warp undefined); callers
+// still reconverge after one-lane branches with __syncwarp().
 __device__ __forceinline__ void named_arrive(uint32_t id, uint32_t nthreads)
 {
-    asm volatile("bar.arrive %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
+    asm volatile("barrier.cta.arrive %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
 }
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads)
 {
-    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
+    asm volatile("barrier.cta.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
 }
 
 // Bounded wait: gives up after kWaitPolls suspended polls (~2 s), returning

@@ -105,14 +105,35 @@ def test_prefill_2x1024_carried_state_matches_single_call(gated):
     assert torch.equal(fb, fin1)
 
 
-def test_prefill_deterministic_and_stream():
-    x = make_prefill_inputs(PrefillCase("det", seqlens=[300, 17], hk=2, hv=4, init_state=True,
+LONG_AMONG_TINY = [700] + [1] * 10   # T <= 128 N: the two-stage scan, with an 11-chunk chain
+
+
+@pytest.mark.parametrize("lens", [[300, 17], [70, 1, 64, 129, 5, 300, 2, 63] * 3, LONG_AMONG_TINY],
+                         ids=["two_long", "24_short", "long_among_tiny"])
+def test_prefill_deterministic_and_stream(lens):
+    """Repeated calls, and a call on a side stream, agree bit for bit: every
+    record a kernel writes is complete before the kernel that reads it, and
+    no stage is refilled under the reads of the chunk before (the last two
+    batches take the two-stage scan, two CTAs per SM; 24 short sequences
+    also take the chunk index)."""
+    x = make_prefill_inputs(PrefillCase("det", seqlens=lens, hk=2, hv=4, init_state=True,
                                         gated_norm=True, seed=10))
     o1, s1 = gpu_prefill(x)
+    for _ in range(8):
+        o3, s3 = gpu_prefill(x)
+        assert np.array_equal(o1, o3) and np.array_equal(s1, s3)
     st = torch.cuda.Stream()
     with torch.cuda.stream(st):
         o2, s2 = gpu_prefill(x, stream=st)
     assert np.array_equal(o1, o2) and np.array_equal(s1, s2)
+
+
+def test_prefill_two_stage_scan_long_chain():
+    """A long sequence among single-token ones takes the two-stage scan (two
+    CTAs per SM) through 11 chunks: each chunk's S record, and so the early
+    rows of every chunk's outputs, follows the oracle."""
+    _check(PrefillCase("long_tiny", seqlens=LONG_AMONG_TINY, hk=2, hv=4, init_state=True,
+                       gated_norm=True, seed=14))
 
 
 def test_prefill_many_sequences_use_the_chunk_index():
