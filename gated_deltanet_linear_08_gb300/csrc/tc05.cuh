@@ -174,6 +174,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32])
         r[i] = __uint_as_float(u[i]);
 }
 
+// 16 consecutive fp32 columns of this thread's TMEM lane.
 // Two 32-column loads (addresses ta, tb) in flight together, one wait.
 __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float (&a)[32], float (&b)[32])
 {
