@@ -25,6 +25,7 @@ not facts they print: parity of those choices is unpinned by the pages.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import subprocess
@@ -41,22 +42,52 @@ _lib = None
 L2_EPS = 1e-6
 
 
-def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (OpenMP when available, no fast-math)."""
-    os.makedirs(_BUILD, exist_ok=True)
-    if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
-        return _LIB_PATH
-    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile the oracle with gcc (OpenMP when available, no fast-math).
+    ``src``/``out`` build another copy of the source: the mutation test
+    compiles the oracle with one planted mistake that way."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(src)):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
     base = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
-            "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
+            "-shared", "-fPIC", "-o", tmp, src, "-lm"]
     try:
         subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
                        capture_output=True)
     except subprocess.CalledProcessError:
         subprocess.run(base, check=True, capture_output=True)
-    os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+    os.replace(tmp, out)
+    return out
+
+
+def _configure(lib):
+    """Declare the C signatures on a loaded oracle library."""
+    P = ctypes.c_void_p
+    i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+    lib.gdn_oracle_softplus.argtypes = [f64]
+    lib.gdn_oracle_softplus.restype = f64
+    lib.gdn_oracle_sigmoid.argtypes = [f64]
+    lib.gdn_oracle_sigmoid.restype = f64
+    lib.gdn_oracle_prep.argtypes = [i64, i32, i32, i32, P, P, P, P, P, P, f64,
+                                    P, P, P, P]
+    lib.gdn_oracle_prep.restype = None
+    lib.gdn_oracle_gated_rmsnorm.argtypes = [i64, i32, P, P, P, f64]
+    lib.gdn_oracle_gated_rmsnorm.restype = None
+    lib.gdn_oracle_core.argtypes = [i32, P, i32, i32, i32, i32, P, P, P, P, P, P,
+                                    P, P, i32]
+    lib.gdn_oracle_core.restype = i32
+    lib.gdn_oracle_core_chunked.argtypes = [i32, P, i32, i32, i32, i32, i32, P, P,
+                                            P, P, P, P, P, P, i32]
+    lib.gdn_oracle_core_chunked.restype = i32
+    lib.gdn_oracle_prefill.argtypes = [i32, P, i32, i32, i32, i32, P, P, P, P, P,
+                                       P, P, f64, P, P, P, f64, P, P, i32]
+    lib.gdn_oracle_prefill.restype = i32
+    lib.gdn_oracle_decode_step.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P,
+                                           P, P, f64, P, P, P, f64, P, i32]
+    lib.gdn_oracle_decode_step.restype = i32
+    return lib
 
 
 def _load():
@@ -64,32 +95,23 @@ def _load():
     with _lock:
         if _lib is None:
             build()
-            lib = ctypes.CDLL(_LIB_PATH)
-            P = ctypes.c_void_p
-            i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
-            lib.gdn_oracle_softplus.argtypes = [f64]
-            lib.gdn_oracle_softplus.restype = f64
-            lib.gdn_oracle_sigmoid.argtypes = [f64]
-            lib.gdn_oracle_sigmoid.restype = f64
-            lib.gdn_oracle_prep.argtypes = [i64, i32, i32, i32, P, P, P, P, P, P, f64,
-                                            P, P, P, P]
-            lib.gdn_oracle_prep.restype = None
-            lib.gdn_oracle_gated_rmsnorm.argtypes = [i64, i32, P, P, P, f64]
-            lib.gdn_oracle_gated_rmsnorm.restype = None
-            lib.gdn_oracle_core.argtypes = [i32, P, i32, i32, i32, i32, P, P, P, P, P, P,
-                                            P, P, i32]
-            lib.gdn_oracle_core.restype = i32
-            lib.gdn_oracle_core_chunked.argtypes = [i32, P, i32, i32, i32, i32, i32, P, P,
-                                                    P, P, P, P, P, P, i32]
-            lib.gdn_oracle_core_chunked.restype = i32
-            lib.gdn_oracle_prefill.argtypes = [i32, P, i32, i32, i32, i32, P, P, P, P, P,
-                                               P, P, f64, P, P, P, f64, P, P, i32]
-            lib.gdn_oracle_prefill.restype = i32
-            lib.gdn_oracle_decode_step.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P,
-                                                   P, P, f64, P, P, P, f64, P, i32]
-            lib.gdn_oracle_decode_step.restype = i32
-            _lib = lib
+            _lib = _configure(ctypes.CDLL(_LIB_PATH))
     return _lib
+
+
+@contextlib.contextmanager
+def library(path: str):
+    """Inside the block every function of this module runs on the library at
+    ``path`` (another build of the oracle's source, e.g. a planted mistake)."""
+    global _lib
+    lib = _configure(ctypes.CDLL(path))
+    with _lock:
+        old, _lib = _lib, lib
+    try:
+        yield
+    finally:
+        with _lock:
+            _lib = old
 
 
 def _c(x, dtype=np.float64):
