@@ -396,13 +396,19 @@ def test_conv_split_sequence_carries_the_state():
 
 
 def test_conv_inputs_channel_order_is_q_k_v():
+    """The channels are q heads, then k heads, then v heads: weights that pass
+    the current token on one block of channels only reproduce exactly that
+    input (through SiLU) and leave the other two zero."""
     T, hk, hv, d = 5, 2, 4, 128
     q = RNG.standard_normal((T, hk, d)); k = RNG.standard_normal((T, hk, d)); v = RNG.standard_normal((T, hv, d))
     C = 2 * hk * d + hv * d
-    w = np.zeros((C, 4)); w[2 * hk * d:, 3] = 1.0      # only the v channels pass the current token
-    qc, kc, vc, _ = oracle.conv_inputs(np.array([0, T]), q, k, v, w)
-    assert np.all(qc == 0) and np.all(kc == 0)
-    assert np.array_equal(vc, oracle.round_bf16(v / (1 + np.exp(-v))))
+    blocks = {"q": (0, hk * d), "k": (hk * d, 2 * hk * d), "v": (2 * hk * d, C)}
+    for name, (lo, hi) in blocks.items():
+        w = np.zeros((C, 4)); w[lo:hi, 3] = 1.0        # only this block passes the current token
+        got = dict(zip("qkv", oracle.conv_inputs(np.array([0, T]), q, k, v, w)[:3]))
+        for other, x in (("q", q), ("k", k), ("v", v)):
+            want = oracle.round_bf16(x / (1 + np.exp(-x))) if other == name else np.zeros_like(x)
+            assert np.array_equal(got[other], want), (name, other)
 
 
 def test_conv_tie_nudging_makes_fp32_and_fp64_roundings_agree():

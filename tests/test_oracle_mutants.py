@@ -125,3 +125,79 @@ def test_planted_mistake_fails_a_pin(tmp_path, name, find, repl):
     failed = _failing_pins(tmp_path, src.replace(find, repl, 1))
     assert failed, f"the oracle with '{name}' planted passes every pin"
     print(name, "caught by", failed)
+
+
+# ---------------------------------------------------------------------------
+# The conv half of the oracle is Python (oracle/__init__.py): a mutated copy
+# of the module is executed and its conv functions stand in for the real ones
+# while the conv pins run.
+# ---------------------------------------------------------------------------
+CONV_MUTANTS = [
+    ("conv_weights_reversed",
+     "acc += w[:, j][None, :] * xe[j:j + T]",
+     "acc += w[:, K - 1 - j][None, :] * xe[j:j + T]"),
+    ("conv_without_silu",
+     "return round_bf16(silu(acc)), xe[T:T + K - 1]",
+     "return round_bf16(acc), xe[T:T + K - 1]"),
+    ("conv_state_ignored",
+     "prev = np.zeros((K - 1, C)) if state is None else np.asarray(state, dtype=np.float64)",
+     "prev = np.zeros((K - 1, C))"),
+    ("conv_new_state_from_the_front",
+     "xe[T:T + K - 1] if K > 1",
+     "xe[0:K - 1] if K > 1"),
+    ("bf16_rounding_truncates",
+     "np.rint(m * 256.0) / 256.0",
+     "np.trunc(m * 256.0) / 256.0"),
+    ("bf16_rounding_seven_bits",
+     "np.rint(m * 256.0) / 256.0",
+     "np.rint(m * 128.0) / 128.0"),
+    ("silu_sign",
+     "return x / (1.0 + np.exp(-x))",
+     "return x / (1.0 + np.exp(x))"),
+    ("conv_channels_k_before_q",
+     "qc = y[:, :hk * d].reshape(T, hk, d)\n    kc = y[:, hk * d:2 * hk * d].reshape(T, hk, d)",
+     "kc = y[:, :hk * d].reshape(T, hk, d)\n    qc = y[:, hk * d:2 * hk * d].reshape(T, hk, d)"),
+]
+
+CONV_PINS = [
+    pins.test_round_bf16_matches_torch_for_fp32_values,
+    pins.test_conv_impulse_weights_give_silu_and_shifts,
+    pins.test_conv_matches_numpy_convolve_per_channel,
+    pins.test_conv_split_sequence_carries_the_state,
+    pins.test_conv_inputs_channel_order_is_q_k_v,
+]
+CONV_FUNCS = ("round_bf16", "silu", "causal_conv_silu", "conv_inputs")
+
+
+def _failing_conv_pins(monkeypatch, source):
+    import types
+    mod = types.ModuleType("oracle_copy")
+    mod.__file__ = oracle.__file__
+    exec(compile(source, "oracle_copy", "exec"), mod.__dict__)
+    for f in CONV_FUNCS:
+        monkeypatch.setattr(oracle, f, getattr(mod, f))
+    failed = []
+    for fn in CONV_PINS:
+        try:
+            fn()
+        except Exception:   # an assertion, or a mistake that breaks the shapes
+            failed.append(fn.__name__)
+    return failed
+
+
+def _py_source():
+    with open(oracle.__file__) as f:
+        return f.read()
+
+
+def test_unchanged_conv_copy_passes_every_conv_pin(monkeypatch):
+    assert _failing_conv_pins(monkeypatch, _py_source()) == []
+
+
+@pytest.mark.parametrize("name,find,repl", CONV_MUTANTS, ids=[m[0] for m in CONV_MUTANTS])
+def test_planted_conv_mistake_fails_a_pin(monkeypatch, name, find, repl):
+    src = _py_source()
+    assert find in src, f"mutation site of {name} not found"
+    failed = _failing_conv_pins(monkeypatch, src.replace(find, repl, 1))
+    assert failed, f"the conv oracle with '{name}' planted passes every conv pin"
+    print(name, "caught by", failed)
