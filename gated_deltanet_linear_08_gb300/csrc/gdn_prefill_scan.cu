@@ -276,16 +276,6 @@ scan_kernel(PrefillArgs p)
             uint4 bc[2];
             bc[0] = *reinterpret_cast<const uint4 *>(stage + kStBc + sw64_chunk_offset(row, 2 * cg));
             bc[1] = *reinterpret_cast<const uint4 *>(stage + kStBc + sw64_chunk_offset(row, 2 * cg + 1));
-            // The loader refills this stage by TMA (the async proxy) once it is
-            // free: the generic reads of Bc and e^{G_last} above are ordered
-            // before that write only by a proxy fence, not by the mbarrier.
-            // Without it, with two CTAs per SM, a refill now and then landed
-            // under these reads and S(c+1) took chunk c+2's Bc.
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&s->sfree[st]);
-            __syncwarp();   // whole warp again before the barrier in put_state
             const __half2 *hp = reinterpret_cast<const __half2 *>(bc);
 #pragma unroll
             for (int j = 0; j < kCols / 2; ++j) {
@@ -293,8 +283,21 @@ scan_kernel(PrefillArgs p)
                 S[2 * j] = fmaf(g, S[2 * j], dv[2 * j] + f2.x);
                 S[2 * j + 1] = fmaf(g, S[2 * j + 1], dv[2 * j + 1] + f2.y);
             }
+            // The loader refills this stage by TMA (the async proxy) once it is
+            // free: the generic reads of Bc and e^{G_last} above are ordered
+            // before that write only by a proxy fence, not by the mbarrier.
+            // Without it, with two CTAs per SM, a refill now and then landed
+            // under these reads and S(c+1) took chunk c+2's Bc.  put_state's
+            // fence serves both its S writes and these reads, and the stage
+            // is released after it, off the chain.
             if (c + 1 < nck)
                 put_state((c + 1) & 1);
+            else
+                fence_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&s->sfree[st]);
+            __syncwarp();
         }
         if (over)
             set_status(p.status, kStatusRange);
