@@ -18,10 +18,13 @@
 // workspace, where the output kernel, fully parallel over chunks, turns it
 // into the chunk's outputs.
 //
-// Roles (10 warps):
+// Roles (11 warps):
 //   warps 0-7   state: warp w holds TMEM lane quadrant w % 4 = state rows
 //               32 (w % 4) .. +31 and value columns 16 (w / 4) .. +15
-//   warp 8      issues every MMA and the copy of S to the workspace
+//   warps 8, 10 issue the MMAs of the first and second 64-row K half of the
+//               state into two accumulators (issuing them is the chain's
+//               largest cost, and two issuing threads overlap it), which the
+//               state threads add; warp 8 also copies S to the workspace
 //   warp 9      issues the stage copies (four stages, or two for short
 //               sequences: Mc, this CTA's Bc slice, e^{G_last}), then
 //               rolls this CTA's share of the carried conv state
@@ -36,12 +39,13 @@ namespace gdn {
 
 namespace {
 
-constexpr int kThreads = 10 * 32;
+constexpr int kThreads = 11 * 32;
 constexpr int kStateWarps = 8;
 constexpr int kIssuerWarp = 8;
 constexpr int kLoaderWarp = 9;
+constexpr int kIssuer2Warp = 10;   // the second K half's MMAs
 // Named barrier (id, participating threads): state warps arrive, the issuer syncs.
-constexpr uint32_t kBarS = 1, kCntS = kStateWarps * 32 + 32;   // S operand written
+constexpr uint32_t kBarS = 1, kCntS = kStateWarps * 32 + 64;   // S operand written
 constexpr int kNv = 32;                 // value columns per CTA
 constexpr int kTiles = kD / kNv;        // 4 CTAs per (sequence, head)
 constexpr int kCols = 16;               // value columns per thread
@@ -53,7 +57,8 @@ constexpr uint32_t kStageBytes = 41984;
 constexpr uint32_t kLoadBytes = 32768 + 8192 + 16;
 
 // TMEM columns: chain accumulators at 0 / 32.
-constexpr uint32_t kTmemCols = 64;
+constexpr uint32_t kTmemCols = 128;
+constexpr uint32_t kAccHalf = 64;   // the second K half's accumulators
 
 // NS stages of copies ahead of the chain: four (one CTA per SM) hide the
 // copies behind long sequences; two (two CTAs per SM) suit batches of short
@@ -104,13 +109,13 @@ __device__ __forceinline__ bool wait_quick(Small *s, uint64_t *bar, uint32_t par
 // Descriptors of the stage operands (shared-memory byte address `st`).
 __device__ __forceinline__ uint64_t desc_k128(uint32_t addr) { return make_desc(addr, 16, 1024, kSw128); }
 
-// D = Mc S over the two 64-wide K halves of the state.
-__device__ __forceinline__ void issue_mcs(uint32_t d, uint32_t st, uint64_t ds, uint32_t idesc)
+// D = Mc S over one 64-wide K half of the state (4 MMAs).
+__device__ __forceinline__ void issue_mcs(uint32_t d, uint32_t st, uint64_t ds, uint32_t idesc, int half)
 {
-    const uint64_t a0 = desc_k128(st + (uint32_t)kWsMc0), a1 = desc_k128(st + (uint32_t)kWsMc1);
+    const uint64_t a = desc_k128(st + (uint32_t)(half ? kWsMc1 : kWsMc0));
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk)
-        mma_f16(d, (kk < 4 ? a0 : a1) + (uint64_t)((kk & 3) * 2), ds + (uint64_t)(kk * 64), idesc, kk != 0);
+    for (int kk = 0; kk < 4; ++kk)
+        mma_f16(d, a + (uint64_t)(kk * 2), ds + (uint64_t)((4 * half + kk) * 64), idesc, kk != 0);
 }
 
 template <int NS>
@@ -140,9 +145,9 @@ scan_kernel(PrefillArgs p)
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&s->full[i], 1);
-            mbar_init(&s->sfree[i], kStateWarps + 1);
+            mbar_init(&s->sfree[i], kStateWarps + 2);
         }
-        mbar_init(&s->bar_chain, 1);
+        mbar_init(&s->bar_chain, 2);
         mbar_fence_init();
         s->fail = 0;
     }
@@ -158,17 +163,21 @@ scan_kernel(PrefillArgs p)
     const uint32_t tbase = s->tmem_base;
     const uint32_t idesc = make_idesc_f16(128, kNv, false, true);
 
-    if (warp == kIssuerWarp) {
-        // ------------------------------------------------------------ issuer
+    if (warp == kIssuerWarp || warp == kIssuer2Warp) {
+        // ----------------------------------------------------------- issuers
+        // each issues one K half's MMAs into its own accumulator; the first
+        // also copies S to the workspace
+        const int half = warp == kIssuer2Warp;
         for (int c = 0; c < nck; ++c) {
             const int b = c & 1, st = c % kStages;   // S operand and accumulator buffer; stage
             const uint32_t sst = sbase + st * kStageBytes;
-            const uint32_t dS = tbase + b * kNv;
+            const uint32_t dS = tbase + half * kAccHalf + b * kNv;
             bool ok = true;
             if (lane == 0) {
                 // the copy of S(c-1) has read its buffer before this chunk's
                 // chain releases the state warps to write S(c+1) there
-                bulk_wait_read<0>();
+                if (!half)
+                    bulk_wait_read<0>();
                 ok = wait_quick(s, &s->full[st], (uint32_t)(c / kStages) & 1, p.status, 1);
             }
             __syncwarp();
@@ -176,16 +185,17 @@ scan_kernel(PrefillArgs p)
             if (lane == 0) {
                 if (ok && !failed(s)) {
                     tc_fence_after();
-                    issue_mcs(dS, sst, make_desc(sbase + kOffS + b * 8192, 512, 512, kSw64), idesc);
+                    issue_mcs(dS, sst, make_desc(sbase + kOffS + b * 8192, 512, 512, kSw64), idesc, half);
                 }
                 mma_commit(&s->bar_chain);
                 mma_commit(&s->sfree[st]);
                 // S(c) -> workspace, for the output kernel
-                bulk_s2g(record(c) + kWsS + r * 8192, sm + kOffS + b * 8192, 8192);
+                if (!half)
+                    bulk_s2g(record(c) + kWsS + r * 8192, sm + kOffS + b * 8192, 8192);
             }
             __syncwarp();
         }
-        if (lane == 0)
+        if (lane == 0 && !half)
             bulk_wait_all();   // every S copy complete before exit (the output kernel reads them)
         __syncwarp();
     } else if (warp == kLoaderWarp) {
@@ -271,7 +281,7 @@ scan_kernel(PrefillArgs p)
             __syncwarp();   // converged for the .aligned TMEM load
             tc_fence_after();
             float dv[kCols];
-            tmem_ld16(tlane + (c & 1) * kNv, dv);
+            tmem_ld16_sum2(tlane + (c & 1) * kNv, tlane + kAccHalf + (c & 1) * kNv, dv);
             const float g = *reinterpret_cast<const float *>(stage + kStScal);
             uint4 bc[2];
             bc[0] = *reinterpret_cast<const uint4 *>(stage + kStBc + sw64_chunk_offset(row, 2 * cg));

@@ -221,6 +221,28 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&r)[16])
         r[i] = __uint_as_float(u[i]);
 }
 
+// The sum of two 16-column TMEM loads (addresses ta, tb): both in flight
+// together, one wait.
+__device__ __forceinline__ void tmem_ld16_sum2(uint32_t ta, uint32_t tb, float (&r)[16])
+{
+    uint32_t u[16], v[16];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
+                 "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                 "{%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];\n\t"
+                 "tcgen05.wait::ld.sync.aligned;"
+                 : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]),
+                   "=r"(u[6]), "=r"(u[7]), "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]),
+                   "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15]),
+                   "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
+                   "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]),
+                   "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+                 : "r"(ta), "r"(tb) : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        r[i] = __uint_as_float(u[i]) + __uint_as_float(v[i]);
+}
+
 // 8 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&r)[8])
 {
