@@ -136,6 +136,35 @@ def test_prefill_two_stage_scan_long_chain():
                        gated_norm=True, seed=14))
 
 
+def _sub_batch(x, first, last):
+    """Sequences first .. last-1 of a packed batch as a batch of their own."""
+    cu = x["cu_seqlens"]
+    s, e = int(cu[first]), int(cu[last])
+    y = dict(x)
+    y["seqlens"] = x["seqlens"][first:last]
+    y["cu_seqlens"] = (cu[first:last + 1] - s).to(torch.int32)
+    for key in ("q", "k", "v", "a", "b", "z"):
+        y[key] = None if x[key] is None else x[key][s:e].contiguous()
+    y["init_state"] = None if x["init_state"] is None else x["init_state"][first:last].contiguous()
+    return y, s, e
+
+
+def test_prefill_units_past_the_output_kernels_unit_list():
+    """640 sequences of 128 tokens at Hv=32: 40960 (chunk, head) units, about
+    270 per output-kernel CTA, so each CTA locates its units past the first
+    256 on the way instead of from the list it builds up front.  Sequences
+    at both ends of the batch (the last ones are all past the list) follow
+    the oracle run on them alone."""
+    x = make_prefill_inputs(PrefillCase("units", seqlens=[128] * 640, hk=16, hv=32, gated_norm=True,
+                                        seed=21))
+    go, gs = gpu_prefill(x)
+    for first, last in ((0, 2), (636, 640)):
+        sub, s, e = _sub_batch(x, first, last)
+        ro, rs = oracle_prefill(sub)
+        assert_out_close(go[s:e], ro, f"units {first}-{last} out")
+        assert_state_close(gs[first:last], rs, f"units {first}-{last} state")
+
+
 def test_prefill_many_sequences_use_the_chunk_index():
     """40 packed sequences (empty, single-token, boundary and multi-chunk
     lengths): from 16 sequences on, the kernels find their chunks through the
