@@ -221,6 +221,15 @@ def job_rate(units_per_rank: float, world: int, ms: float) -> float:
     return world * units_per_rank / (ms * 1e-3)
 
 
+def spread(ms):
+    """p10, median and p90 of per-call times (nearest rank)."""
+    s = sorted(ms)
+    if not s:
+        return None
+    pick = lambda f: s[min(len(s) - 1, max(0, round(f * (len(s) - 1))))]
+    return {"p10": pick(0.1), "median": statistics.median(s), "p90": pick(0.9)}
+
+
 def timed_region(gdn, pre, dec, steps, warmup, stream, world):
     x, shared, sets = pre
     eps = x["eps"]
@@ -332,8 +341,9 @@ def e2e_region(gdn, x, dec_y, dev, steps, warmup, stream):
 # ---------------------------------------------------------------------------
 # CPU legs: the fp64 oracle as it stands, on the host cores
 # ---------------------------------------------------------------------------
-def _oracle_prefill_sample(T: int):
-    """Oracle prefill on the first T tokens of the T=2048 workload (all 32 heads)."""
+def _oracle_prefill_sample(T: int, nthreads: int = 0):
+    """Oracle prefill on the first T tokens of the T=2048 workload (all 32
+    heads), on `nthreads` host threads (0: all cores)."""
     import oracle
     from gated_deltanet_linear_08_gb300.inputs import to_f64
     x = make_prefill_inputs(CASE_T2048)
@@ -344,7 +354,7 @@ def _oracle_prefill_sample(T: int):
 
     def run():
         oracle.prefill(cu, f["q"], f["k"], f["v"], f["a"], f["b"], f["A_log"], f["dt_bias"],
-                       None, f["z"], f["norm_w"], eps=x["eps"], nthreads=os.cpu_count())
+                       None, f["z"], f["norm_w"], eps=x["eps"], nthreads=nthreads or os.cpu_count())
     return run
 
 
@@ -471,12 +481,17 @@ def cpu_baseline(seconds: float = 10.0):
     repeated for a third of that."""
     reps, tp = _repeat_for(_oracle_prefill_sample(2048), seconds)
     dreps, td = _repeat_for(_oracle_decode_sample(CASE_DECODE.batch), seconds / 3)
+    # one core: the first 512 tokens (the recurrence costs the same per token)
+    sreps, ts = _repeat_for(_oracle_prefill_sample(512, nthreads=1), seconds / 3)
     return {"value": 2048 / tp, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"fp64 oracle, the full T=2048 prefill (32 heads, gated norm) x {reps} "
                       f"({reps * tp:.1f} s); decode: the 256-sequence step x {dreps} ({dreps * td:.1f} s)",
             "seconds": round(reps * tp, 2),
             "decode": {"value": decode_state_bytes(CASE_DECODE.batch) / td / 1e9, "unit": "GB/s",
-                       "tokens_per_s": CASE_DECODE.batch / td, "seconds": round(dreps * td, 2)}}
+                       "tokens_per_s": CASE_DECODE.batch / td, "seconds": round(dreps * td, 2)},
+            "single_core": {"value": 512 / ts, "unit": "tokens/s", "cores": 1,
+                            "sample": f"the first 512 tokens (32 heads, gated norm) x {sreps}",
+                            "seconds": round(sreps * ts, 2)}}
 
 
 def reference_arm(args, rank):
@@ -585,11 +600,11 @@ def main():
                      "peak_kind": f"{peaks['src']} bf16 burst",
                      "work": f"{flops} algorithmic flop per call "
                              f"({PREFILL_FLOP_PER_TOKEN_HEAD} per token per value head)"},
-        "prefill": {"ms_per_call": pre_mean, "algorithmic_bytes": pre_bytes,
+        "prefill": {"ms_per_call": pre_mean, "ms_spread": spread(pre_ms), "algorithmic_bytes": pre_bytes,
                     "hbm_gbs": pre_bytes / (pre_mean * 1e-3) / 1e9,
                     "hbm_frac": pre_bytes / (pre_mean * 1e-3) / 1e9 / peaks["hbm"],
                     "workspace_bytes": gdn.workspace_bytes(1, T, 16, hv)},
-        "decode": {"value": world * dec_gbs, "unit": "GB/s", "ms_per_call": dec_mean,
+        "decode": {"value": world * dec_gbs, "unit": "GB/s", "ms_per_call": dec_mean, "ms_spread": spread(dec_ms),
                    "tokens_per_s": world * CASE_DECODE.batch / (dec_mean * 1e-3),
                    "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm"],
                                 "unit": "GB/s", "frac": dec_gbs / peaks["hbm"],
