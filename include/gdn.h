@@ -90,7 +90,10 @@ size_t gdn_prefill_workspace_bytes(const gdn_shape_t *shape);
  *   workspace   device scratch of at least gdn_prefill_workspace_bytes(shape)
  *               bytes, 1024-byte aligned, owned by the caller; its contents
  *               need no initialisation and are garbage afterwards.  Calls that
- *               share one workspace must be ordered on the GPU.
+ *               share one workspace must be ordered on the GPU.  It must not
+ *               overlap any input (the kernels write it while reading them):
+ *               overlaps with out and final_state are rejected, overlaps with
+ *               the inputs are not checked and give wrong results.
  * Returns GDN_OK once the work is enqueued.
  */
 gdn_status_t gdn_prefill(const gdn_shape_t *shape,
