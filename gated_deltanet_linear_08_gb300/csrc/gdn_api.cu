@@ -5,6 +5,8 @@
 // candidate", maintainer review: unsupported shapes handled explicitly).
 // Nothing here allocates device memory, prints, aborts or synchronises,
 // except gdn_check_device_status, which is documented as off the hot path.
+#include <atomic>
+
 #include <cuda_runtime.h>
 
 #include "../../include/gdn.h"
@@ -16,20 +18,25 @@ namespace {
 __device__ uint32_t g_device_status;
 
 constexpr int kMaxDevices = 64;
-uint32_t *g_status_ptr[kMaxDevices];   // device address of g_device_status, per device
+// Device address of g_device_status, per device.  Host threads may make their
+// first call on a device at the same time: each then looks the address up and
+// stores the same value, which the atomic makes a well-defined race.
+std::atomic<uint32_t *> g_status_ptr[kMaxDevices];
 
 uint32_t *status_ptr()
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return nullptr;
-    if (!g_status_ptr[dev]) {
+    uint32_t *cached = g_status_ptr[dev].load(std::memory_order_relaxed);
+    if (!cached) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess)
             return nullptr;
-        g_status_ptr[dev] = static_cast<uint32_t *>(p);
+        cached = static_cast<uint32_t *>(p);
+        g_status_ptr[dev].store(cached, std::memory_order_relaxed);
     }
-    return g_status_ptr[dev];
+    return cached;
 }
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -188,16 +195,24 @@ gdn_status_t gdn_prefill_conv(const gdn_shape_t *s, const gdn_strides_t *strides
     const size_t hk = s->hk, hv = s->hv;
     const size_t out_b = T * hv * 128 * 2;
     const size_t st_b = N * hv * 128 * 128 * 4;
+    // everything the call reads; the workspace, out and final_state (the
+    // buffers it writes) may overlap none of them, except that final_state
+    // may be exactly init_state (the in-place case)
     const struct { const void *p; size_t n; } ins[] = {
         {q, span(q, T, hk, in.q, 128)}, {k, span(k, T, hk, in.k, 128)}, {v, span(v, T, hv, in.v, 128)},
         {a, span(a, T, hv, in.a, 1)}, {b, span(b, T, hv, in.b, 1)}, {z, span(z, T, hv, in.z, 128)},
-        {init_state, init_state ? st_b : 0}, {cu_seqlens, (N + 1) * 4}, {workspace, need}};
+        {init_state, init_state ? st_b : 0}, {cu_seqlens, (N + 1) * 4}, {A_log, hv * 4}, {dt_bias, hv * 4},
+        {norm_w, z ? 256u : 0u}};
     for (const auto &x : ins)
-        if (overlaps(out, out_b, x.p, x.n))
+        if (overlaps(out, out_b, x.p, x.n) || overlaps(workspace, need, x.p, x.n))
+            return GDN_ERR_INVALID_ARG;
+    for (const auto &x : ins)   // ins[6] is init_state, checked below
+        if (&x != &ins[6] && overlaps(final_state, st_b, x.p, x.n))
             return GDN_ERR_INVALID_ARG;
     if (init_state != final_state && overlaps(final_state, st_b, init_state, init_state ? st_b : 0))
         return GDN_ERR_INVALID_ARG;   // partial overlap; exact equality is the in-place case
-    if (overlaps(final_state, st_b, out, out_b) || overlaps(final_state, st_b, workspace, need))
+    if (overlaps(final_state, st_b, out, out_b) || overlaps(final_state, st_b, workspace, need)
+        || overlaps(out, out_b, workspace, need))
         return GDN_ERR_INVALID_ARG;
     gdn::ConvArgs cv;
     size_t cs_b = 0;
@@ -208,12 +223,19 @@ gdn_status_t gdn_prefill_conv(const gdn_shape_t *s, const gdn_strides_t *strides
         for (const auto &x : ins)
             if (overlaps(cv.state_out, cs_b, x.p, x.n))
                 return GDN_ERR_INVALID_ARG;
-        if (overlaps(cv.state_out, cs_b, out, out_b) || overlaps(cv.state_out, cs_b, final_state, st_b))
+        if (overlaps(cv.state_out, cs_b, out, out_b) || overlaps(cv.state_out, cs_b, final_state, st_b)
+            || overlaps(cv.state_out, cs_b, workspace, need))
             return GDN_ERR_INVALID_ARG;
     }
     if (overlaps(cv.state_in, cs_b, out, out_b) || overlaps(cv.state_in, cs_b, final_state, st_b)
         || overlaps(cv.state_in, cs_b, workspace, need))
         return GDN_ERR_INVALID_ARG;
+    if (conv) {
+        const size_t wb = (size_t)cv.channels * cv.width * 2;
+        if (overlaps(cv.weight, wb, out, out_b) || overlaps(cv.weight, wb, final_state, st_b)
+            || overlaps(cv.weight, wb, workspace, need))
+            return GDN_ERR_INVALID_ARG;
+    }
 
     gdn::PrefillArgs p{};
     p.num_seqs = s->num_seqs;
@@ -309,12 +331,18 @@ gdn_status_t gdn_decode_conv(const gdn_shape_t *s, const gdn_strides_t *strides,
         return GDN_ERR_ALIGNMENT;
     const size_t hk = s->hk, hv = s->hv, BT = B * (size_t)tokens;
     const size_t out_b = BT * hv * 256;
+    const size_t pool_b = (size_t)num_slots * hv * 128 * 128 * 4;
     const struct { const void *p; size_t n; } ins[] = {
         {q, span(q, BT, hk, in.q, 128)}, {k, span(k, BT, hk, in.k, 128)}, {v, span(v, BT, hv, in.v, 128)},
         {a, span(a, BT, hv, in.a, 1)}, {b, span(b, BT, hv, in.b, 1)}, {z, span(z, BT, hv, in.z, 128)},
-        {state, (size_t)num_slots * hv * 128 * 128 * 4}, {state_idx, state_idx ? B * 4 : 0}};
+        {state, pool_b}, {state_idx, state_idx ? B * 4 : 0}, {A_log, hv * 4}, {dt_bias, hv * 4},
+        {norm_w, z ? 256u : 0u}};
     for (const auto &x : ins)
         if (overlaps(out, out_b, x.p, x.n))
+            return GDN_ERR_INVALID_ARG;
+    // the pool is read and written in place: no other input may lie in it
+    for (const auto &x : ins)   // ins[6] is the pool itself
+        if (&x != &ins[6] && overlaps(state, pool_b, x.p, x.n))
             return GDN_ERR_INVALID_ARG;
     gdn::ConvArgs cv;
     size_t cs_b = 0;

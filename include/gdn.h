@@ -90,10 +90,12 @@ size_t gdn_prefill_workspace_bytes(const gdn_shape_t *shape);
  *   workspace   device scratch of at least gdn_prefill_workspace_bytes(shape)
  *               bytes, 1024-byte aligned, owned by the caller; its contents
  *               need no initialisation and are garbage afterwards.  Calls that
- *               share one workspace must be ordered on the GPU.  It must not
- *               overlap any input (the kernels write it while reading them):
- *               overlaps with out and final_state are rejected, overlaps with
- *               the inputs are not checked and give wrong results.
+ *               share one workspace must be ordered on the GPU.
+ * Aliasing: out, final_state and the workspace (everything the call writes)
+ * must not overlap one another or any input (q, k, v, a, b, z, norm_w,
+ * A_log, dt_bias, init_state, cu_seqlens; strided inputs by the bytes their
+ * strides span), with one exception: final_state may be exactly init_state.
+ * Any other overlap returns GDN_ERR_INVALID_ARG before any launch.
  * Returns GDN_OK once the work is enqueued.
  */
 gdn_status_t gdn_prefill(const gdn_shape_t *shape,
@@ -116,10 +118,12 @@ gdn_status_t gdn_prefill(const gdn_shape_t *shape,
  *
  * Arguments and results are those of gdn_prefill without the workspace: the
  * scratch lives in a fixed 64 MiB array of device memory that the library
- * holds on every GPU that loads it, until the process exits (about 850
- * packed tokens at Hv = 32).  A shape whose
+ * holds on every GPU that loads it, until the process exits.  A shape whose
  * gdn_prefill_workspace_bytes exceeds 64 MiB returns GDN_ERR_WORKSPACE
- * before any launch.  Nothing in the array needs clearing between calls.
+ * before any launch.  With the workspace formula that limit is
+ * ceil(T_tot/64) + N <= 14 at Hv = 32 (one sequence of up to 832 tokens,
+ * fewer tokens with more sequences) and <= 9 at Hv = 48.  Nothing in the
+ * array needs clearing between calls.
  * The first call on a device looks up the array's device address (with that
  * device current); make that first call before any stream capture.  Every
  * call on a device shares the one array, so calls that may overlap on the
@@ -146,7 +150,8 @@ gdn_status_t gdn_prefill_noalloc(const gdn_shape_t *shape,
  *   state  fp32 [B, Hv, 128, 128], read and overwritten in place
  *   z      bf16 [B, Hv, 128] or NULL (no epilogue); norm_w bf16 [128]; eps
  *   out    bf16 [B, Hv, 128]; must not overlap any input or the state
- * Needs no workspace.
+ * The state must not overlap any other input either; an overlap returns
+ * GDN_ERR_INVALID_ARG before any launch.  Needs no workspace.
  */
 gdn_status_t gdn_decode(const gdn_shape_t *shape,
                         const void *q, const void *k, const void *v,
@@ -179,6 +184,7 @@ gdn_status_t gdn_decode(const gdn_shape_t *shape,
  *   z        bf16 [B, tokens, Hv, 128] or NULL (no epilogue); norm_w, eps
  *            as gdn_decode
  *   out      bf16 [B, tokens, Hv, 128]; must not overlap any input or the pool
+ *            (nor may the pool overlap any other input: GDN_ERR_INVALID_ARG)
  * gdn_decode(shape, ...) is gdn_decode_slots with tokens = 1, no index and
  * num_slots = B.
  */
@@ -277,8 +283,12 @@ size_t gdn_prefill_conv_workspace_bytes(const gdn_shape_t *shape);
  * gdn_prefill_strided.  The conv runs as its own pass over all tokens and
  * writes its output into the workspace, which must hold
  * gdn_prefill_conv_workspace_bytes (else GDN_ERR_WORKSPACE); the core then
- * reads it there.  The carried states are rolled once every read of the old
- * ones has finished, so state_out may be state_in. */
+ * reads it there.  After the call that output, y bf16 [T_tot][C] (rows of
+ * q | k | v channels), starts at byte gdn_prefill_workspace_bytes(shape) of
+ * the workspace, so a caller may inspect the core's actual inputs.  The
+ * carried states are rolled once every read of the old ones has finished,
+ * so state_out may be state_in.  The conv weight and states follow the
+ * aliasing rule of gdn_prefill (they are inputs; state_out is written). */
 gdn_status_t gdn_prefill_conv(const gdn_shape_t *shape, const gdn_strides_t *strides,
                               const gdn_conv_t *conv,
                               const void *q, const void *k, const void *v,

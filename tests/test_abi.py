@@ -212,3 +212,71 @@ def test_missing_library_fails_loudly(tmp_path):
             B.load(str(tmp_path / "nope.so"))
     finally:
         B._lib = saved
+
+
+def _no_device():
+    """True when no CUDA device is visible: then a call that passes every host
+    check stops at the device lookup with GDN_ERR_CUDA, before any launch,
+    which lets the tests below show that the one changed pointer is what a
+    rejected call trips on.  (With a GPU present such a call would launch on
+    the fake pointers, so it is never made.)"""
+    import torch
+    return not torch.cuda.is_available()
+
+
+def test_prefill_rejects_writes_over_inputs(lib):
+    """The workspace, out and final_state are written while the inputs are
+    read: any overlap with an input is refused on the host (pegainfer page,
+    Correctness: alias handling)."""
+    ok = B.make_shape(1, 64, 16, 32)
+    z, w = FAKE + 0xB0000000, FAKE + 0xC0000000
+    if _no_device():
+        assert _prefill(lib, ok) == 4                        # every host check passes
+        assert _prefill(lib, ok, z=z, w=w) == 4
+        assert _prefill(lib, ok, init=FAKE + 0x90000000) == 4   # in place: final_state == init_state
+    for name, base in (("q", 0), ("k", 0x10000000), ("v", 0x20000000), ("a", 0x30000000), ("b", 0x40000000),
+                       ("A_log", 0x50000000), ("dt_bias", 0x60000000), ("cu", 0x70000000)):
+        assert _prefill(lib, ok, ws=FAKE + base) == 1, name            # workspace starts on the input
+        assert _prefill(lib, ok, ws=FAKE + base - 0x400) == 1, name    # and one that ends in it
+        assert _prefill(lib, ok, fin=FAKE + base) == 1, name           # final_state over the input
+    assert _prefill(lib, ok, z=z, w=w, ws=z) == 1                      # workspace over z
+    assert _prefill(lib, ok, z=z, w=w, ws=w - 0x400) == 1              # ... over the norm weights
+    assert _prefill(lib, ok, z=z, w=w, fin=w) == 1                     # final_state over the norm weights
+    assert _prefill(lib, ok, init=FAKE + 0xD0000000, ws=FAKE + 0xD0000000) == 1   # ... over init_state
+    assert _prefill(lib, ok, init=FAKE + 0xD0000000, fin=FAKE + 0xD0000400) == 1  # partial state overlap
+    assert _prefill(lib, ok, out=FAKE + 0xA0000000) == 1               # out over the workspace
+
+
+def test_decode_rejects_a_pool_over_inputs(lib):
+    def dec(shape, **kw):
+        a = dict(q=FAKE, k=FAKE + 0x10000000, v=FAKE + 0x20000000, a=FAKE + 0x30000000,
+                 b=FAKE + 0x40000000, A_log=FAKE + 0x50000000, dt=FAKE + 0x60000000,
+                 state=FAKE + 0x70000000, idx=FAKE + 0x80000000, z=None, w=None, eps=1e-6,
+                 out=FAKE + 0x90000000)
+        a.update(kw)
+        return lib.gdn_decode_slots(ctypes.byref(shape), 2, 8, a["q"], a["k"], a["v"], a["a"], a["b"], a["A_log"],
+                                    a["dt"], a["state"], a["idx"], a["z"], a["w"], a["eps"], a["out"], None)
+    sh = B.make_shape(4, 8, 16, 32)
+    if _no_device():
+        assert dec(sh) == 4
+    for name, base in (("q", 0), ("v", 0x20000000), ("a", 0x30000000), ("A_log", 0x50000000),
+                       ("dt_bias", 0x60000000), ("state_idx", 0x80000000)):
+        assert dec(sh, state=FAKE + base) == 1, name
+    assert dec(sh, z=FAKE + 0xA0000000, w=FAKE + 0xB0000000, state=FAKE + 0xA0000000) == 1   # over z
+
+
+def test_prefill_conv_rejects_writes_over_its_weights(lib):
+    W = FAKE + 0xC0000000
+    shape = B.make_shape(1, 64, 16, 32)
+
+    def pre(ws=FAKE + 0xA0000000, out=FAKE + 0x80000000, fin=FAKE + 0x90000000):
+        cv = B.Conv(4, W, None, None)
+        return lib.gdn_prefill_conv(ctypes.byref(shape), None, ctypes.byref(cv), FAKE, FAKE + 0x10000000,
+                                    FAKE + 0x20000000, FAKE + 0x30000000, FAKE + 0x40000000, FAKE + 0x50000000,
+                                    FAKE + 0x60000000, None, FAKE + 0x70000000, None, None, 1e-6, out, fin, ws,
+                                    1 << 40, None)
+    if _no_device():
+        assert pre() == 4
+    assert pre(ws=W) == 1
+    assert pre(out=W) == 1
+    assert pre(fin=W) == 1
