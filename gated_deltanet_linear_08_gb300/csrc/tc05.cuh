@@ -243,20 +243,6 @@ __device__ __forceinline__ void tmem_ld16_sum2(uint32_t ta, uint32_t tb, float (
         r[i] = __uint_as_float(u[i]) + __uint_as_float(v[i]);
 }
 
-// 8 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&r)[8])
-{
-    uint32_t u[8];
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
-                 "tcgen05.wait::ld.sync.aligned;"
-                 : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]),
-                   "=r"(u[6]), "=r"(u[7])
-                 : "r"(taddr) : "memory");
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        r[i] = __uint_as_float(u[i]);
-}
-
 // ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
@@ -304,42 +290,6 @@ __device__ __forceinline__ bool mbar_test(uint64_t *mbar, uint32_t parity)
     return ok != 0;
 }
 
-// Wait with cluster-scope acquire (pairs with remote release arrivals).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *mbar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(ok) : "r"(smem_u32(mbar)), "r"(parity), "n"(kSuspendNs) : "memory");
-    return ok != 0;
-}
-// Arrive, with cluster-scope release, on the mbarrier at the same offset in
-// the shared memory of CTA `rank` of this cluster.
-__device__ __forceinline__ void mbar_arrive_remote(uint64_t *local_mbar, uint32_t rank)
-{
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local_mbar)), "r"(rank));
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(remote) : "memory");
-}
-// Asynchronous 4-byte store into the shared memory of CTA `rank` of this
-// cluster, completing 4 transaction bytes on that CTA's mbarrier at the same
-// offset as `local_mbar` (no fence needed: the receiver waits on its barrier).
-__device__ __forceinline__ void st_async_remote(const void *local_dst, float v, uint64_t *local_mbar,
-                                                uint32_t rank)
-{
-    uint32_t rd, rb;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rd) : "r"(smem_u32(local_dst)), "r"(rank));
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_u32(local_mbar)), "r"(rank));
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
-                 :: "r"(rd), "r"(__float_as_uint(v)), "r"(rb) : "memory");
-}
-__device__ __forceinline__ uint32_t cluster_ctarank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
 // Named CTA barriers: producers arrive without waiting, the consumer syncs.
 // The non-.aligned forms, which do not require the warp to arrive converged
 // (the .aligned bar.arrive / bar.sync leave a split warp undefined); callers
