@@ -11,6 +11,8 @@
 // host code its name is only a host-side stand-in, never a device address;
 // the device address comes from cudaGetSymbolAddress, looked up once per
 // device (with that device current) on the first call made on it.
+#include <atomic>
+
 #include <cuda_runtime.h>
 
 #include "../../include/gdn.h"
@@ -18,14 +20,18 @@
 
 namespace {
 
-// 64 MiB: each (64-token chunk, value head) takes 137 KB of scratch, so at
-// Hv = 32 this covers 14 chunks, about 850 packed tokens.  The extra 1 KB
+// 64 MiB.  The workspace takes one record per (64-token chunk, value head)
+// for ceil(T/64) + N chunks, plus the chunk index, so at Hv = 32 this covers
+// ceil(T/64) + N <= 14 (one sequence of up to 832 tokens).  The extra 1 KB
 // lets the base be rounded up to the 1024-byte alignment gdn_prefill requires.
 constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes + 1024];
 
 constexpr int kMaxDevices = 64;
-void *g_scratch_ptr[kMaxDevices];   // device address of g_noalloc_scratch, per device
+// Device address of g_noalloc_scratch, per device.  Two host threads making
+// their first call on one device at the same time both look it up and store
+// the same value; the atomic keeps that race well defined.
+std::atomic<void *> g_scratch_ptr[kMaxDevices];
 
 }  // namespace
 
@@ -42,13 +48,13 @@ extern "C" gdn_status_t gdn_prefill_noalloc(const gdn_shape_t *s, const void *q,
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return GDN_ERR_CUDA;
-    if (!g_scratch_ptr[dev]) {
-        void *ptr = nullptr;
+    void *ptr = g_scratch_ptr[dev].load(std::memory_order_relaxed);
+    if (!ptr) {
         if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr)
             return GDN_ERR_CUDA;
-        g_scratch_ptr[dev] = ptr;
+        g_scratch_ptr[dev].store(ptr, std::memory_order_relaxed);
     }
-    uintptr_t base = reinterpret_cast<uintptr_t>(g_scratch_ptr[dev]);
+    uintptr_t base = reinterpret_cast<uintptr_t>(ptr);
     base = (base + 1023) & ~uintptr_t(1023);
     return gdn_prefill(s, q, k, v, a, b, A_log, dt_bias, init_state, cu_seqlens, z, norm_w, eps,
                        out, final_state, reinterpret_cast<void *>(base), kNoAllocScratchBytes, stream);
