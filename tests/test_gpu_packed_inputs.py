@@ -107,3 +107,85 @@ def test_conv_reads_inputs_from_a_packed_projection():
     torch.cuda.synchronize()
     assert torch.equal(o_g, o_r) and torch.equal(pool_g, pool_r) and torch.equal(cp_g, cp_r)
     assert gdn.check_device_status() == 0
+
+
+def _pack_in_order(tensors: dict, order):
+    """One [tokens..., W] buffer holding the named blocks in `order` per token,
+    and strided views of it shaped like the dense tensors."""
+    lead = tensors["q"].shape[:-2]
+    flat = {n: (t.flatten(-2) if t.dim() == len(lead) + 2 else t) for n, t in tensors.items()}
+    W = sum(flat[n].shape[-1] for n in order)
+    buf = torch.zeros(*lead, W + (-W) % 8, dtype=torch.bfloat16, device=tensors["q"].device)
+    views, off = {}, 0
+    for n in order:
+        m = flat[n].shape[-1]
+        buf[..., off:off + m] = flat[n]
+        views[n] = buf[..., off:off + m]
+        if tensors[n].dim() == len(lead) + 2:
+            views[n] = views[n].unflatten(-1, tensors[n].shape[-2:])
+        off += m
+        off += (-off) % 8 if n in ("a", "b") else 0   # keep the next 128-wide block 16-byte aligned
+    return buf, views
+
+
+ORDER = ("a", "z", "v", "b", "k", "q")   # not the q | k | v | z | b | a of the projection
+
+
+def test_prefill_packed_hv48_against_the_oracle():
+    """Packed inputs in a non-default block order, Hv = 48 (three value heads
+    per k head): the outputs and final states follow the fp64 oracle."""
+    import gated_deltanet_linear_08_gb300 as gdn
+    from parity_util import assert_out_close, assert_state_close, oracle_prefill
+    x = make_prefill_inputs(PrefillCase("packed_hv48", seqlens=[300, 1, 129, 64], hk=16, hv=48, init_state=True,
+                                        gated_norm=True, seed=35))
+    d = to_dev(x)
+    buf, vw = _pack_in_order({n: d[n] for n in ("q", "k", "v", "z", "a", "b")}, ORDER)
+    assert not vw["q"].is_contiguous() and vw["q"].stride(0) == buf.shape[-1]
+    out, fin = gdn.prefill(vw["q"], vw["k"], vw["v"], vw["a"], vw["b"], d["A_log"], d["dt_bias"], d["cu_seqlens"],
+                           init_state=d["init_state"], z=vw["z"], norm_w=d["norm_w"], eps=x["eps"])
+    torch.cuda.synchronize()
+    assert gdn.check_device_status() == 0
+    ro, rs = oracle_prefill(x)
+    assert_out_close(out.double().cpu().numpy(), ro, "packed_hv48 prefill out")
+    assert_state_close(fin.double().cpu().numpy(), rs, "packed_hv48 prefill state")
+
+
+def test_decode_packed_hv48_against_the_oracle():
+    """Slot-pool decode of 3 draft tokens with packed inputs in a non-default
+    block order at Hv = 48: outputs and states follow the fp64 oracle token
+    by token."""
+    import numpy as np
+
+    import gated_deltanet_linear_08_gb300 as gdn
+    import oracle
+    from gated_deltanet_linear_08_gb300.inputs import to_f64
+    from parity_util import DECODE_STATE_REL, assert_out_close, record
+    case = DecodeSlotsCase("packed_dec_hv48", batch=24, tokens=3, slots=32, skipped=2, hk=16, hv=48,
+                           gated_norm=True, seed=36)
+    x = make_decode_slots_inputs(case)
+    dev = "cuda"
+    t = {n: x[n].to(dev) for n in ("q", "k", "v", "a", "b", "z")}
+    pool = x["pool"].to(dev)
+    buf, vw = _pack_in_order(t, ORDER)
+    out = gdn.decode_slots(vw["q"], vw["k"], vw["v"], vw["a"], vw["b"], x["A_log"].to(dev), x["dt_bias"].to(dev),
+                           pool, state_idx=x["state_idx"].to(dev), z=vw["z"], norm_w=x["norm_w"].to(dev),
+                           eps=x["eps"])
+    torch.cuda.synchronize()
+    assert gdn.check_device_status() == 0
+    idx = x["state_idx"].numpy()
+    live = np.nonzero(idx >= 0)[0]
+    S = np.ascontiguousarray(to_f64(x["pool"])[idx[live]])
+    T = case.tokens
+    ref = np.zeros((len(live), T, case.hv, 128))
+    for s in range(T):
+        ref[:, s] = oracle.decode_step(*(to_f64(x[n])[live, s] for n in ("q", "k", "v", "a", "b")),
+                                       to_f64(x["A_log"]), to_f64(x["dt_bias"]), S, z=to_f64(x["z"])[live, s],
+                                       norm_w=to_f64(x["norm_w"]), eps=x["eps"])
+    got = out.double().cpu().numpy()
+    assert_out_close(got[live], ref, "packed_dec_hv48 out")
+    assert np.all(got[idx < 0] == 0)
+    Sg = pool.cpu()[torch.as_tensor(idx[live].astype(np.int64))].double().numpy()
+    rel = float(np.abs(Sg - S).max() / np.abs(S).max())
+    record("packed_dec_hv48 state", "state", dict(max_abs=rel, violations=int(rel > DECODE_STATE_REL)),
+           f"max|dS|/max|S| <= {DECODE_STATE_REL:g}")
+    assert rel <= DECODE_STATE_REL
