@@ -33,10 +33,10 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from gated_deltanet_linear_08_gb300.inputs import (CASE_DECODE, CASE_T2048, DecodeCase,  # noqa: E402
-                                                   DecodeSlotsCase, PrefillCase, conv_channels, make_conv_inputs,
-                                                   make_decode_inputs, make_decode_slots_inputs,
-                                                   make_prefill_inputs)
+from gated_deltanet_linear_08_gb300.inputs import (CASE_8x128, CASE_DECODE, CASE_T64, CASE_T2048,  # noqa: E402
+                                                   CASE_VARLEN48, DecodeCase, DecodeSlotsCase, PrefillCase,
+                                                   conv_channels, make_conv_inputs, make_decode_inputs,
+                                                   make_decode_slots_inputs, make_prefill_inputs)
 
 METRIC = "GDN prefill tokens/s & decode GB/s at Hv=32,D=128; % of tensor/HBM roofline"
 PREFILL_FLOP_PER_TOKEN_HEAD = 10 * 64 * 128 + 6 * 128 * 128   # 180,224 (C=64 chunked count)
@@ -421,6 +421,58 @@ def time_calls(call, calls: int, warmup: int, stream) -> float:
     return start.elapsed_time(end) / calls
 
 
+def prefill_bytes(T: int, N: int, hk: int, hv: int, gated: bool, init: bool) -> int:
+    """Algorithmic HBM bytes of one prefill call: q, k, v, a, b read and the
+    bf16 output written once per token (z too with the epilogue), the final
+    states written and the initial states read once per sequence."""
+    per_tok = 2 * hk * 256 + hv * 256 + 2 * hv * 2 + hv * 256 + (hv * 256 if gated else 0)
+    return T * per_tok + N * hv * 128 * 128 * 4 * (2 if init else 1)
+
+
+L2_FLUSH_BYTES = 256 << 20   # twice the 129 MB L2
+
+
+def prefill_config_region(gdn, case: PrefillCase, dev, stream, peaks, calls: int = 20, warmup: int = 3):
+    """One of the other prefill workloads: the device time of each call by
+    CUDA events on the launching stream, with L2 flushed between calls
+    (outside the events), so every call reads its inputs from HBM."""
+    x = make_prefill_inputs(case)
+    d = {k: (None if x[k] is None else x[k].to(dev)) for k in
+         ("q", "k", "v", "a", "b", "A_log", "dt_bias", "init_state", "cu_seqlens", "z", "norm_w")}
+    T, N, hk, hv = x["q"].shape[0], len(x["seqlens"]), case.hk, case.hv
+    out = torch.empty(T, hv, 128, dtype=torch.bfloat16, device=dev)
+    fin = torch.empty(N, hv, 128, 128, dtype=torch.float32, device=dev)
+    ws = gdn.alloc_workspace(N, T, hk, hv, dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def call():
+        gdn.prefill(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["cu_seqlens"],
+                    init_state=d["init_state"], z=d["z"], norm_w=d["norm_w"], eps=x["eps"], out=out,
+                    final_state=fin, workspace=ws, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            call()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(calls)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            call()
+            b.record(stream)
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    mean = sum(ms) / len(ms)
+    flops = T * hv * PREFILL_FLOP_PER_TOKEN_HEAD
+    nbytes = prefill_bytes(T, N, hk, hv, case.gated_norm, case.init_state)
+    return {"workload": f"{N} sequence(s), {T} tokens, Hk/Hv = {hk}/{hv}"
+                        + (", initial states" if case.init_state else "")
+                        + (", gated RMSNorm" if case.gated_norm else ""),
+            "ms_per_call": mean, "ms_spread": spread(ms), "tokens_per_s": T / (mean * 1e-3),
+            "tensor_frac": flops / (mean * 1e-3) / 1e12 / peaks["bf16"],
+            "hbm_frac": nbytes / (mean * 1e-3) / 1e9 / peaks["hbm"],
+            "algorithmic_flop": flops, "algorithmic_bytes": nbytes,
+            "l2": "flushed between calls (256 MiB written outside the events)"}
+
+
 CONV_WIDTH = 4
 
 
@@ -616,6 +668,11 @@ def main():
         "gpu_launches": 4 * args.steps,
         "clocks": clk.summary(),
     }
+    line["prefill_configs"] = {}
+    for case in (CASE_T64, CASE_8x128, CASE_VARLEN48):
+        r = prefill_config_region(gdn, case, dev, stream, peaks)
+        r["ms_per_call"] = max_over_ranks(r["ms_per_call"], world)
+        line["prefill_configs"][case.name] = r
     pk_ms = max_over_ranks(packed_prefill_region(gdn, pre, stream), world)
     line["prefill_packed_inputs"] = {
         "workload": "the same T=2048 prefill, inputs read in place from a packed [T, 12352] projection buffer",
