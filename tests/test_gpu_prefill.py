@@ -105,7 +105,7 @@ def test_prefill_2x1024_carried_state_matches_single_call(gated):
     assert torch.equal(fb, fin1)
 
 
-LONG_AMONG_TINY = [700] + [1] * 10   # T <= 128 N: the two-stage scan, with an 11-chunk chain
+LONG_AMONG_TINY = [700] + [1] * 10   # an 11-chunk chain among single-token ones
 
 
 @pytest.mark.parametrize("lens", [[300, 17], [70, 1, 64, 129, 5, 300, 2, 63] * 3, LONG_AMONG_TINY],
@@ -113,9 +113,8 @@ LONG_AMONG_TINY = [700] + [1] * 10   # T <= 128 N: the two-stage scan, with an 1
 def test_prefill_deterministic_and_stream(lens):
     """Repeated calls, and a call on a side stream, agree bit for bit: every
     record a kernel writes is complete before the kernel that reads it, and
-    no stage is refilled under the reads of the chunk before (the last two
-    batches take the two-stage scan, two CTAs per SM; 24 short sequences
-    also take the chunk index)."""
+    no stage is refilled under the reads of the chunk before (24 short
+    sequences also take the chunk index)."""
     x = make_prefill_inputs(PrefillCase("det", seqlens=lens, hk=2, hv=4, init_state=True,
                                         gated_norm=True, seed=10))
     o1, s1 = gpu_prefill(x)
@@ -128,10 +127,10 @@ def test_prefill_deterministic_and_stream(lens):
     assert np.array_equal(o1, o2) and np.array_equal(s1, s2)
 
 
-def test_prefill_two_stage_scan_long_chain():
-    """A long sequence among single-token ones takes the two-stage scan (two
-    CTAs per SM) through 11 chunks: each chunk's S record, and so the early
-    rows of every chunk's outputs, follows the oracle."""
+def test_prefill_long_chain_among_tiny_ones():
+    """A long sequence among single-token ones, 11 chunks on one chain: each
+    chunk's S record, and so the early rows of every chunk's outputs, follows
+    the oracle."""
     _check(PrefillCase("long_tiny", seqlens=LONG_AMONG_TINY, hk=2, hv=4, init_state=True,
                        gated_norm=True, seed=14))
 
@@ -220,3 +219,23 @@ def test_prefill_malformed_seqlens_are_flagged_and_skipped(nseq):
     assert_out_close(out.double().cpu().numpy(), ro, f"bad{nseq} out")
     assert_state_close(fin[:N - 1].double().cpu().numpy(), rs, f"bad{nseq} state")
     assert torch.equal(fin[N - 1], init[N - 1])
+
+
+def test_prefill_more_chains_than_scan_ctas():
+    """48 sequences at Hv=32: 6144 chains (sequence, head, value slice), far
+    more than fit on the GPU at once, so every scan CTA runs about 40 chains
+    in turn (the stages and S buffers carried over chain boundaries, the next
+    chain's initial state loaded during the current one).  Sequences at both
+    ends of the batch follow the oracle run on them alone, and a repeat of
+    the call agrees bit for bit."""
+    lens = [1, 63, 64, 65, 130, 200] * 8
+    x = make_prefill_inputs(PrefillCase("chains", seqlens=lens, hk=16, hv=32, init_state=True, gated_norm=True,
+                                        seed=22))
+    go, gs = gpu_prefill(x)
+    go2, gs2 = gpu_prefill(x)
+    assert np.array_equal(go, go2) and np.array_equal(gs, gs2)
+    for first, last in ((0, 3), (45, 48)):
+        sub, s, e = _sub_batch(x, first, last)
+        ro, rs = oracle_prefill(sub)
+        assert_out_close(go[s:e], ro, f"chains {first}-{last} out")
+        assert_state_close(gs[first:last], rs, f"chains {first}-{last} state")

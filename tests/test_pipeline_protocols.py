@@ -3,7 +3,8 @@
 Each role of the scan kernel and of the output kernel is written here as a
 sequence of the waits, arrivals and asynchronous operations it issues, with
 the same barrier counts, parities and buffer indices as the CUDA source
-(csrc/gdn_prefill_scan.cu, csrc/gdn_prefill_out.cu).  A random scheduler
+(csrc/gdn_prefill_scan.cu, csrc/gdn_prefill_out.cu; the scan CTA runs its
+chains in turn, counting steps over all of them).  A random scheduler
 interleaves the roles and completes the asynchronous operations (tensor-map
 and bulk copies in any order, each thread's tcgen05 commits in issue order)
 at random times, for many seeds and sizes.  It checks that:
@@ -268,7 +269,18 @@ def test_output_kernel_protocol(nj, norm, whole):
 # ---------------------------------------------------------------------------
 
 def scan_protocol(sim, nck, NS, issuers=2, state_warps=8):
+    """The persistent scan CTA: `nck` is the chunk count of one chain or a
+    list of them (the chains the CTA runs in turn).  Every role counts the
+    steps g over all chains; buffers, stages and parities follow g."""
     B = sim.buf
+    lens = [nck] if isinstance(nck, int) else list(nck)
+    nck = sum(lens)   # total steps
+    firsts = set()    # steps that start a chain
+    g = 0
+    for L in lens:
+        if L:
+            firsts.add(g)
+        g += L
     full = [MBar(f"full{i}", 1) for i in range(NS)]
     sfree = [MBar(f"sfree{i}", state_warps + issuers) for i in range(NS)]
     chain = MBar("chain", issuers)
@@ -320,9 +332,9 @@ def scan_protocol(sim, nck, NS, issuers=2, state_warps=8):
             B.end_write(f"S{c & 1}", (c, w))
             bar_s.arrive(c)
 
-        if nck > 0:
-            yield ("do", lambda: put(0))
         for c in range(nck):
+            if c in firsts:   # a chain starts: its initial state is the operand of its first step
+                yield ("do", lambda c=c: put(c))
             st = c % NS
             yield wait(full[st], c // NS)
             yield wait(chain, c)
@@ -336,7 +348,7 @@ def scan_protocol(sim, nck, NS, issuers=2, state_warps=8):
             def update(c=c, st=st):
                 for ii in range(issuers):
                     B.end_read(f"acc{ii}_{c & 1}", c, f"state{w}")
-                if c + 1 < nck:
+                if c + 1 < nck and c + 1 not in firsts:   # the chain goes on
                     put(c + 1)
                 B.end_read(f"stage{st}", c, f"state{w}")   # released after the fence
                 sfree[st].arrive()
@@ -369,12 +381,25 @@ def _scan_buffers_hold_whole_states(sim):
 
 
 @pytest.mark.parametrize("nck", [1, 2, 3, 4, 5, 8, 11])
-@pytest.mark.parametrize("NS", [2, 4])
+@pytest.mark.parametrize("NS", [4])
 def test_scan_kernel_protocol(nck, NS):
     for seed in range(40):
         sim = Sim(random.Random(100 * nck + 7 * seed + NS))
         _scan_buffers_hold_whole_states(sim)
         scan_protocol(sim, nck, NS)
+        sim.run()
+
+
+@pytest.mark.parametrize("lens", [[1, 1, 1], [2, 0, 3], [3, 1, 0, 2, 5], [1, 4, 1, 4], [0, 0, 2]],
+                         ids=lambda l: "-".join(map(str, l)))
+@pytest.mark.parametrize("NS", [4])
+def test_persistent_scan_runs_chains_in_turn(lens, NS):
+    """A CTA running several chains back to back (empty ones included): the
+    stages and S buffers carry over the chain boundaries by the step count."""
+    for seed in range(40):
+        sim = Sim(random.Random(31 * sum(lens) + 7 * seed + NS + len(lens)))
+        _scan_buffers_hold_whole_states(sim)
+        scan_protocol(sim, lens, NS)
         sim.run()
 
 
@@ -441,5 +466,5 @@ def test_planted_protocol_slip_is_reported(kind, name, find, repl):
                     ns["out_protocol"](sim, size, True, True)
                 else:
                     ns["_scan_buffers_hold_whole_states"](sim)
-                    ns["scan_protocol"](sim, size, 2)
+                    ns["scan_protocol"](sim, size, 4)
                 sim.run()
