@@ -26,7 +26,8 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED",
                 6: "GDN_ERR_WORKSPACE"}
 EXPORTED = ("gdn_status_string", "gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_decode",
             "gdn_check_device_status", "gdn_prefill_noalloc", "gdn_decode_slots", "gdn_prefill_strided",
-            "gdn_decode_strided", "gdn_prefill_conv", "gdn_decode_conv", "gdn_prefill_conv_workspace_bytes")
+            "gdn_decode_strided", "gdn_prefill_conv", "gdn_decode_conv", "gdn_prefill_conv_workspace_bytes",
+            "gdn_conv_prefill")
 
 
 class GdnError(RuntimeError):
@@ -97,6 +98,9 @@ def load(path: Optional[str] = None):
                                             ctypes.c_int32, ctypes.c_int32, P, P, P, P, P, P, P, P, P, P, P, f32,
                                             P, P]
             lib.gdn_decode_conv.restype = ctypes.c_int
+            lib.gdn_conv_prefill.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(Strides), ctypes.POINTER(Conv),
+                                             P, P, P, P, P, P]
+            lib.gdn_conv_prefill.restype = ctypes.c_int
             lib.gdn_check_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
             lib.gdn_check_device_status.restype = ctypes.c_int
             _lib = lib
@@ -248,6 +252,29 @@ def prefill(q, k, v, a, b, A_log, dt_bias, cu_seqlens, init_state=None, z=None, 
         code = load().gdn_prefill_strided(ctypes.byref(shape), ctypes.byref(strides), *ins, *rest)
     _check(code)
     return out, final_state
+
+
+def conv_prefill(q, k, v, cu_seqlens, conv_weight, conv_state=None, y=None, stream=None):
+    """The causal conv1d + SiLU alone through ``gdn_conv_prefill``: returns y
+    [T, Hk*128 + Hk*128 + Hv*128] bf16, the q | k | v rows the prefill's conv
+    feeds to the core (bit for bit).  q, k [T, Hk, 128], v [T, Hv, 128] bf16;
+    conv_weight [C, K] bf16; conv_state [N, K-1, C] bf16 or None (zeros)."""
+    dev = q.device
+    T, hk = q.shape[0], q.shape[1]
+    hv = v.shape[1]
+    N = cu_seqlens.shape[0] - 1
+    C = conv_weight.shape[0]
+    if y is None:
+        y = torch.empty(T, C, dtype=torch.bfloat16, device=dev)
+    shape = make_shape(N, T, hk, hv)
+    strides = _strides(dict(q=q, k=k, v=v, z=None, a=None, b=None), 1)
+    conv = _conv(conv_weight, conv_state, None, dev)
+    code = load().gdn_conv_prefill(ctypes.byref(shape), None if strides is None else ctypes.byref(strides),
+                                   ctypes.byref(conv), _in_ptr(q, "q", dev), _in_ptr(k, "k", dev),
+                                   _in_ptr(v, "v", dev), _ptr(cu_seqlens, torch.int32, "cu_seqlens", dev),
+                                   _ptr(y, torch.bfloat16, "y", dev), _stream_handle(stream, dev))
+    _check(code)
+    return y
 
 
 def prefill_noalloc(q, k, v, a, b, A_log, dt_bias, cu_seqlens, init_state=None, z=None,

@@ -274,6 +274,65 @@ gdn_status_t gdn_prefill_conv(const gdn_shape_t *s, const gdn_strides_t *strides
     return gdn::launch_prefill(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+gdn_status_t gdn_conv_prefill(const gdn_shape_t *s, const gdn_strides_t *strides, const gdn_conv_t *conv,
+                              const void *q, const void *k, const void *v, const int32_t *cu_seqlens, void *y,
+                              void *stream)
+{
+    gdn_status_t st = check_shape(s);
+    if (st != GDN_OK)
+        return st;
+    const size_t T = (size_t)s->total_tokens, N = (size_t)s->num_seqs;
+    if (N == 0)
+        return T == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
+    if (!conv || !cu_seqlens)
+        return GDN_ERR_INVALID_ARG;
+    if (conv->state_out)
+        return GDN_ERR_INVALID_ARG;   // this entry point writes y only
+    if (T == 0)
+        return GDN_OK;
+    if (!q || !k || !v || !y)
+        return GDN_ERR_INVALID_ARG;
+    // only q, k and v are read: the caller's a, b strides do not matter here
+    gdn_strides_t qkv;
+    if (strides) {
+        qkv = *strides;
+        qkv.a = qkv.b = gdn_stride_t{1, 1};
+    }
+    gdn::InputStrides in;
+    if (!resolve_strides(strides ? &qkv : nullptr, s->hk, s->hv, false, in))
+        return GDN_ERR_INVALID_ARG;
+    const void *al16[] = {q, k, v, y};
+    for (const void *ptr : al16)
+        if (!aligned(ptr, 16))
+            return GDN_ERR_ALIGNMENT;
+    gdn::ConvArgs cv;
+    size_t cs_b = 0;
+    if ((st = resolve_conv(conv, s, N, false, cv, cs_b)) != GDN_OK)
+        return st;
+    const size_t hk = s->hk, hv = s->hv;
+    const size_t y_b = T * (size_t)cv.channels * 2;
+    const struct { const void *p; size_t n; } ins[] = {
+        {q, span(q, T, hk, in.q, 128)}, {k, span(k, T, hk, in.k, 128)}, {v, span(v, T, hv, in.v, 128)},
+        {cu_seqlens, (N + 1) * 4}, {cv.weight, (size_t)cv.channels * cv.width * 2}, {cv.state_in, cs_b}};
+    for (const auto &x : ins)
+        if (overlaps(y, y_b, x.p, x.n))
+            return GDN_ERR_INVALID_ARG;
+    cv.x_q = q; cv.x_k = k; cv.x_v = v;
+    cv.x_in = in;
+    cv.y = static_cast<__nv_bfloat16 *>(y);
+    gdn::PrefillArgs p{};
+    p.num_seqs = s->num_seqs;
+    p.total_tokens = s->total_tokens;
+    p.hk = s->hk;
+    p.hv = s->hv;
+    p.cu_seqlens = cu_seqlens;
+    p.conv = cv;
+    p.status = status_ptr();
+    if (!p.status)
+        return GDN_ERR_CUDA;
+    return gdn::launch_prefill_conv(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 gdn_status_t gdn_prefill_strided(const gdn_shape_t *s, const gdn_strides_t *strides, const void *q,
                                  const void *k, const void *v, const void *a, const void *b, const float *A_log,
                                  const float *dt_bias, const float *init_state, const int32_t *cu_seqlens,

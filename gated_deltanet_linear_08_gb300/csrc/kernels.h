@@ -138,8 +138,9 @@ cudaError_t launch_decode(const DecodeArgs &args, cudaStream_t stream);
 cudaError_t launch_prefill_prep(const PrefillArgs &args, cudaStream_t stream);
 cudaError_t launch_prefill_scan(const PrefillArgs &args, cudaStream_t stream);
 cudaError_t launch_prefill_out(const PrefillArgs &args, cudaStream_t stream);
-// The conv ahead of the prefill core: y = silu(conv(x)) for every token, in
-// stream order before prep (which then reads y through args.q/k/v).
+// The conv ahead of the prefill core: y = silu(conv(x)) for every token into
+// args.conv.y, in stream order before prep (which then reads y through
+// args.q/k/v); also the whole of gdn_conv_prefill.
 cudaError_t launch_prefill_conv(const PrefillArgs &args, cudaStream_t stream);
 // The chunk index args.chunk_off (when set), built before the other kernels.
 cudaError_t launch_chunk_index(const PrefillArgs &args, cudaStream_t stream);

@@ -283,12 +283,10 @@ size_t gdn_prefill_conv_workspace_bytes(const gdn_shape_t *shape);
  * gdn_prefill_strided.  The conv runs as its own pass over all tokens and
  * writes its output into the workspace, which must hold
  * gdn_prefill_conv_workspace_bytes (else GDN_ERR_WORKSPACE); the core then
- * reads it there.  After the call that output, y bf16 [T_tot][C] (rows of
- * q | k | v channels), starts at byte gdn_prefill_workspace_bytes(shape) of
- * the workspace, so a caller may inspect the core's actual inputs.  The
- * carried states are rolled once every read of the old ones has finished,
- * so state_out may be state_in.  The conv weight and states follow the
- * aliasing rule of gdn_prefill (they are inputs; state_out is written). */
+ * reads it there.  That output is exactly what gdn_conv_prefill writes.  The
+ * carried states are rolled once every read of the old ones has finished, so
+ * state_out may be state_in.  The conv weight and states follow the aliasing
+ * rule of gdn_prefill (they are inputs; state_out is written). */
 gdn_status_t gdn_prefill_conv(const gdn_shape_t *shape, const gdn_strides_t *strides,
                               const gdn_conv_t *conv,
                               const void *q, const void *k, const void *v,
@@ -299,6 +297,19 @@ gdn_status_t gdn_prefill_conv(const gdn_shape_t *shape, const gdn_strides_t *str
                               void *out, float *final_state,
                               void *workspace, size_t workspace_bytes,
                               void *stream);
+
+/* gdn_conv_prefill -- the causal conv1d + SiLU alone over packed sequences
+ * (the definition above): y bf16 [T_tot][C], dense, the rows of q | k | v
+ * channels, from the raw q, k, v (strided as in gdn_prefill_strided;
+ * strides NULL: dense) and the carried states conv->state_in (NULL: zeros).
+ * It is the pass gdn_prefill_conv runs ahead of the core, so its values are
+ * bit for bit the core's inputs there, which a caller can inspect or reuse.  conv->state_out must
+ * be NULL (this entry point writes y only; GDN_ERR_INVALID_ARG otherwise);
+ * y must not overlap any input.  Needs no workspace. */
+gdn_status_t gdn_conv_prefill(const gdn_shape_t *shape, const gdn_strides_t *strides,
+                              const gdn_conv_t *conv,
+                              const void *q, const void *k, const void *v,
+                              const int32_t *cu_seqlens, void *y, void *stream);
 
 /* gdn_decode_strided with the conv ahead of the core; conv->state_in is the
  * conv-state pool, indexed like state_pool.  Skipped and out-of-pool

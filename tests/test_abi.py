@@ -280,3 +280,25 @@ def test_prefill_conv_rejects_writes_over_its_weights(lib):
     assert pre(ws=W) == 1
     assert pre(out=W) == 1
     assert pre(fin=W) == 1
+
+
+def test_conv_prefill_rejects_bad_arguments(lib):
+    """gdn_conv_prefill writes y only: a state_out, a y over an input, or a
+    bad descriptor is refused on the host."""
+    W, S = FAKE + 0xC0000000, FAKE + 0xD0000000
+    shape = B.make_shape(1, 64, 16, 32)
+
+    def call(width=4, weight=W, sin=S, sout=None, y=FAKE + 0x80000000, cu=FAKE + 0x70000000):
+        cv = B.Conv(width, weight, sin, sout)
+        return lib.gdn_conv_prefill(ctypes.byref(shape), None, ctypes.byref(cv), FAKE, FAKE + 0x10000000,
+                                    FAKE + 0x20000000, cu, y, None)
+    if _no_device():
+        assert call() == 4                    # every host check passes
+    assert call(sout=S) == 1                  # this entry point writes no state
+    assert call(width=0) == 1
+    assert call(weight=None) == 1
+    assert call(cu=None) == 1
+    assert call(y=None) == 1
+    assert call(y=FAKE + 0x20000000) == 1     # y over v
+    assert call(y=W) == 1                     # y over the weights
+    assert call(y=FAKE + 0x80000000 + 8) == 3

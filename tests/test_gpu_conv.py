@@ -7,10 +7,10 @@ The conv output is rounded to bf16 on both sides; the kernels sum in fp32 and
 the oracle in fp64, so an element whose exact value sits within the fp32
 evaluation error of a bf16 rounding midpoint may round either way: both are
 correct roundings, the conv's result is not unique there.  So each test
-  1. reads the conv outputs the GPU actually produced (the prefill writes
-     them into its workspace; for decode, whose conv runs in registers, the
-     prefill conv pass on the same raw tokens and states gives them, and a
-     bitwise check shows that decode computes exactly those values),
+  1. takes the conv outputs the GPU produces: gdn_conv_prefill writes them
+     out, and bitwise checks show that the prefill with the conv and the
+     decode with its conv in registers compute exactly those values (their
+     results equal the plain path's on them, bit for bit),
   2. checks that every one is a valid rounding of the exact fp64 value
      (parity_util.conv_check_rounding) and counts the ties rounded the other
      way,
@@ -58,22 +58,24 @@ def _check_roundings(what, y_gpu, X, cu, w, states):
 
 
 def _gpu_prefill_conv(x, cv, in_place=False):
-    """gdn.prefill with the conv, on a workspace allocated here so that the
-    conv outputs the core ran on can be read back from it."""
+    """gdn.prefill with the conv; the conv outputs from gdn.conv_prefill, and
+    the plain prefill on them, which must give the conv call's results bit for
+    bit."""
     import gated_deltanet_linear_08_gb300 as gdn
     d = to_dev(x)
-    T, hk, hv, N = x["q"].shape[0], x["q"].shape[1], x["v"].shape[1], len(x["seqlens"])
+    hk, hv = x["q"].shape[1], x["v"].shape[1]
     w = cv["weight"].cuda()
     st = None if cv["state"] is None else cv["state"].cuda()
-    ws = gdn.alloc_workspace(N, T, hk, hv, "cuda", conv=True)
+    y = gdn.conv_prefill(d["q"], d["k"], d["v"], d["cu_seqlens"], w, st)   # before the call rolls st in place
     out, fin, cs = gdn.prefill(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["cu_seqlens"],
                                init_state=d["init_state"], z=d["z"], norm_w=d["norm_w"], eps=x["eps"],
-                               conv_weight=w, conv_state=st, conv_state_out=st if in_place else None, workspace=ws)
+                               conv_weight=w, conv_state=st, conv_state_out=st if in_place else None)
+    yq, yk, yv = (t.contiguous() for t in _split(y, hk, hv))
+    out2, fin2 = gdn.prefill(yq, yk, yv, d["a"], d["b"], d["A_log"], d["dt_bias"], d["cu_seqlens"],
+                             init_state=d["init_state"], z=d["z"], norm_w=d["norm_w"], eps=x["eps"])
     torch.cuda.synchronize()
     assert gdn.check_device_status() == 0
-    core = gdn.workspace_bytes(N, T, hk, hv)
-    C = conv_channels(hk, hv)
-    y = ws[core:core + T * C * 2].view(torch.bfloat16).reshape(T, C)
+    assert torch.equal(out, out2) and torch.equal(fin, fin2), "the prefill's conv differs from gdn_conv_prefill's"
     return out, fin, cs, y.double().cpu().numpy()
 
 
@@ -164,23 +166,15 @@ def test_prefill_conv_in_pieces_matches_one_call():
 
 
 def _gpu_conv_outputs(q, k, v, cu, weight, states):
-    """The conv outputs the prefill conv pass produces for packed raw tokens
-    q, k, v (bf16, [T, H, 128], CPU) of sequences cu with carried states
-    [N, K-1, C]: bf16 [T, C] on the device.  The core of that call is not
-    used (zero gates)."""
+    """The conv outputs gdn_conv_prefill produces for packed raw tokens q, k,
+    v (bf16, [T, H, 128], CPU) of sequences cu with carried states [N, K-1,
+    C]: bf16 [T, C] on the device."""
     import gated_deltanet_linear_08_gb300 as gdn
-    T, hk, hv, N = q.shape[0], q.shape[1], v.shape[1], len(cu) - 1
     dev = "cuda"
-    zeros_ab = torch.zeros(T, hv, dtype=torch.bfloat16, device=dev)
-    zeros_h = torch.zeros(hv, dtype=torch.float32, device=dev)
-    ws = gdn.alloc_workspace(N, T, hk, hv, dev, conv=True)
-    gdn.prefill(q.to(dev), k.to(dev), v.to(dev), zeros_ab, zeros_ab, zeros_h, zeros_h,
-                torch.as_tensor(cu, dtype=torch.int32, device=dev), conv_weight=weight.to(dev),
-                conv_state=states.to(dev) if states.numel() else None, workspace=ws)
+    y = gdn.conv_prefill(q.to(dev), k.to(dev), v.to(dev), torch.as_tensor(cu, dtype=torch.int32, device=dev),
+                         weight.to(dev), states.to(dev) if states.numel() else None)
     torch.cuda.synchronize()
-    core = gdn.workspace_bytes(N, T, hk, hv)
-    C = conv_channels(hk, hv)
-    return ws[core:core + T * C * 2].view(torch.bfloat16).reshape(T, C).clone()
+    return y
 
 
 def _decode_conv(case, width, out_of_place=False):
