@@ -45,17 +45,25 @@ decode_kernel(DecodeArgs p)
     __shared__ float s_red[4];
 
     __nv_bfloat16 *outg = reinterpret_cast<__nv_bfloat16 *>(p.out);
-    const int slot = p.state_idx ? p.state_idx[n] : n;
-    if (slot < 0 || slot >= p.num_slots) {
-        // No state for this sequence (skipped, or out of the pool): zero
-        // outputs.  Every thread of the first four warps stores its column
-        // first; the one-lane status update of an out-of-pool index comes
-        // after the stores.  (With that update ahead of the stores, some
-        // builds of this kernel lost the stores of lanes 1-31 of warp 0.)
+    int slot = n;
+    bool out_of_pool = false;
+    if (p.state_idx) {
+        slot = p.state_idx[n];
+        if (slot >= p.num_slots) {   // out of the pool: flagged and skipped
+            out_of_pool = true;
+            slot = -1;
+        }
+    }
+    if (slot < 0) {
+        // No state for this sequence: zero outputs.  Every thread of the
+        // first four warps stores its column first; the one-lane status
+        // update of an out-of-pool index comes after the stores.  (With that
+        // update ahead of the stores, a build of this kernel lost the stores
+        // of lanes 1-31 of warp 0.)
         if (tid < kD)
             for (int t = 0; t < T; ++t)
                 outg[(((size_t)n * T + t) * hv + h) * kD + tid] = __float2bfloat16_rn(0.f);
-        if (tid == 0 && slot >= p.num_slots)
+        if (out_of_pool && tid == 0)
             set_status(p.status, kStatusRange);
         return;
     }
