@@ -55,7 +55,7 @@ def _run(case):
     return rel
 
 
-@pytest.mark.parametrize("tokens", [1, 2, 3, 8])
+@pytest.mark.parametrize("tokens", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("gated", [False, True])
 def test_decode_slots_multi_token(tokens, gated):
     _run(DecodeSlotsCase(f"slots_T{tokens}", batch=64, tokens=tokens, slots=96, skipped=5,
