@@ -394,8 +394,7 @@ __device__ __forceinline__ void draft_prefetch_ahead(const DecodeArgs &p, int ah
         const int slot = p.state_idx ? p.state_idx[n] : n;
         if (slot >= 0 && slot < p.num_slots) {
             const float *S = p.state + ((size_t)slot * p.hv + h) * (size_t)(kD * kD);
-            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(S), "r"((uint32_t)(kD * kD * sizeof(float)))
-                         : "memory");
+            bulk_prefetch_l2(S, (uint32_t)(kD * kD * sizeof(float)));
         }
     } else if (warp == 5 && lane < 2 * kMaxDraft) {
         const int t = lane >> 1, half = lane & 1;

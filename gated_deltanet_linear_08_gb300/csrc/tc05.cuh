@@ -326,6 +326,13 @@ __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, u
                  : "memory");
 }
 
+// Bulk prefetch of a global range into L2 (address 16-byte aligned, size a
+// multiple of 16); nothing waits for it.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src_gmem, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src_gmem), "r"(bytes) : "memory");
+}
+
 // Bulk shared -> global copy, committed as its own bulk group of the issuing
 // thread (both addresses 16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void bulk_s2g(void *dst_gmem, const void *src_smem, uint32_t bytes)
