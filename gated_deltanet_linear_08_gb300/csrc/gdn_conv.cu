@@ -9,10 +9,15 @@
 // every load and store is a 256-byte coalesced row.  The per-element cost is
 // four fp32 products and a SiLU (an exponential and a reciprocal on the
 // special-function units, whose rate bounds the kernel next to HBM); small
-// threads keep four CTAs per SM so loads and arithmetic overlap.  A run inside one
-// sequence (the common case) issues all its loads at once; a run that a
-// sequence start crosses resets the window from that sequence's carried
-// state.  Grouped q and k heads are convolved once, not once per value head.
+// threads keep four CTAs per SM so loads and arithmetic overlap.  Every
+// thread requests its run's rows and the K-1 rows before them before it looks
+// up the sequence, and each CTA prefetches into L2 the rows of the CTA one
+// resident wave later, so a CTA's loads mostly hit L2 while HBM streams the
+// next wave.  A run that a sequence start crosses (or whose window does)
+// instead resets the window from that sequence's carried state.  Grouped q
+// and k heads are convolved once, not once per value head.
+#include <atomic>
+
 #include "common.cuh"
 #include "conv.cuh"
 #include "kernels.h"
@@ -23,6 +28,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kRun = 8;   // tokens per thread
 constexpr int kCh = 4;    // channels per thread (one 8-byte vector)
+constexpr int kMaxDevices = 64;
 
 // Sequence holding token t: the last n with cu[n] <= t (cu nondecreasing in
 // a well-formed call; otherwise any n in range, which only ever reads
@@ -40,11 +46,29 @@ __device__ __forceinline__ int seq_of(const int32_t *cu, int num_seqs, int t)
     return lo;
 }
 
-template <int KW>
-__global__ void __launch_bounds__(kThreads, 4)
-conv_prefill_kernel(PrefillArgs p)
+// The rows of the CTA `ahead` places later in launch order (about one wave
+// of resident CTAs later) are prefetched into L2: 8 tokens x 16 lines of 128
+// bytes (the CTA's 1024 channels, 8 heads of one of q, k, v), one line per
+// thread of the first 128.
+__device__ __forceinline__ void conv_prefetch_ahead(const PrefillArgs &p, int ahead)
 {
     const ConvArgs &cv = p.conv;
+    const int b = blockIdx.x + blockIdx.y * gridDim.x + ahead;
+    if (ahead <= 0 || b >= gridDim.x * gridDim.y || threadIdx.x >= kRun * 16)
+        return;
+    const int bx = b % gridDim.x, by = b / gridDim.x;
+    const int c = bx * kThreads * kCh + (threadIdx.x & 15) * 64;   // 64 channels per 128-byte line
+    const int t = by * kRun + (threadIdx.x >> 4);
+    if (c < cv.channels && t < p.total_tokens)
+        asm volatile("prefetch.global.L2 [%0];" :: "l"(conv_src(cv.x_q, cv.x_k, cv.x_v, cv.x_in, p.hk, c, t)));
+}
+
+template <int KW>
+__global__ void __launch_bounds__(kThreads, 4)
+conv_prefill_kernel(PrefillArgs p, int ahead)
+{
+    const ConvArgs &cv = p.conv;
+    conv_prefetch_ahead(p, ahead);
     const int c = (blockIdx.x * kThreads + threadIdx.x) * kCh;
     const int t0 = blockIdx.y * kRun;
     if (c >= cv.channels || t0 >= p.total_tokens)
@@ -56,20 +80,30 @@ conv_prefill_kernel(PrefillArgs p)
     __nv_bfloat16 *yb = cv.y + c;
     auto src = [&](int t) { return *reinterpret_cast<const uint2 *>(xb + (int64_t)t * xt); };
 
-    int n = seq_of(p.cu_seqlens, p.num_seqs, t0);
-    int s = p.cu_seqlens[n], e = p.cu_seqlens[n + 1];
-    const bool fast = nt == kRun && t0 >= s && t0 + kRun <= e;   // a full run inside one sequence
-    uint2 raw[kRun];
-    if (fast) {
+    // The run's rows and the K-1 rows before it are requested first, as if
+    // one sequence held them all (the common case); the sequence lookup runs
+    // under those loads.
+    constexpr int kHist = KW > 1 ? KW - 1 : 1;
+    uint2 raw[kRun], pre[kHist];
 #pragma unroll
-        for (int i = 0; i < kRun; ++i)
+    for (int i = 0; i < kRun; ++i)
+        if (i < nt)
             raw[i] = src(t0 + i);
+#pragma unroll
+    for (int j = 0; j < KW - 1; ++j) {
+        const int pos = t0 - (KW - 1) + j;
+        pre[j] = pos >= 0 ? src(pos) : make_uint2(0, 0);
     }
     float w[KW][kCh];
     conv_weights<kCh, KW>(cv.weight, c, w);
 
+    int n = seq_of(p.cu_seqlens, p.num_seqs, t0);
+    int s = p.cu_seqlens[n], e = p.cu_seqlens[n + 1];
+    // a full run whose window lies inside one sequence too
+    const bool fast = nt == kRun && t0 - (KW - 1) >= s && t0 + kRun <= e;
+
     // the K-1 raw inputs before position t of sequence n (which starts at s)
-    float win[KW > 1 ? KW - 1 : 1][kCh];
+    float win[kHist][kCh];
     auto load_window = [&](int t) {
 #pragma unroll
         for (int j = 0; j < KW - 1; ++j) {
@@ -103,13 +137,17 @@ conv_prefill_kernel(PrefillArgs p)
         *reinterpret_cast<uint2 *>(yb + (size_t)t * cv.channels) = make_uint2(pack2(y[0], y[1]), pack2(y[2], y[3]));
     };
 
-    load_window(t0);
     if (fast) {
+#pragma unroll
+        for (int j = 0; j < KW - 1; ++j)
+            unpack4(pre[j], win[j]);
 #pragma unroll
         for (int i = 0; i < kRun; ++i)
             step(raw[i], t0 + i);
     } else {
-        // a sequence starts inside the run (or cu_seqlens do not cover it)
+        // a sequence starts inside the run or its window (or cu_seqlens do
+        // not cover it)
+        load_window(t0);
 #pragma unroll 1
         for (int t = t0; t < t0 + nt; ++t) {
             if (t >= e) {
@@ -127,8 +165,27 @@ conv_prefill_kernel(PrefillArgs p)
 template <int KW>
 cudaError_t launch_width(const PrefillArgs &p, cudaStream_t stream)
 {
+    // prefetch distance: the CTAs resident at once, once per device
+    static std::atomic<int> resident[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    int ahead = resident[dev].load(std::memory_order_relaxed);
+    if (!ahead) {
+        int sms = 0, per_sm = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, conv_prefill_kernel<KW>, kThreads, 0);
+        if (e != cudaSuccess)
+            return e;
+        ahead = sms * (per_sm > 0 ? per_sm : 1);
+        resident[dev].store(ahead, std::memory_order_relaxed);
+    }
     const dim3 grid((p.conv.channels / kCh + kThreads - 1) / kThreads, (p.total_tokens + kRun - 1) / kRun);
-    conv_prefill_kernel<KW><<<grid, kThreads, 0, stream>>>(p);
+    conv_prefill_kernel<KW><<<grid, kThreads, 0, stream>>>(p, ahead);
     return cudaGetLastError();
 }
 
