@@ -197,6 +197,11 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
         set_status(p.status, kStatusBadSeqlens);
     if (!live)
         return;
+    // The scan kernel may be scheduled as soon as every prep CTA has started:
+    // its CTAs take SMs that prep's last wave leaves free and run their
+    // prologue there; griddepcontrol.wait still holds them until this whole
+    // grid has finished and its writes are visible.
+    grid_dep_launch();
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
@@ -679,7 +684,6 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
     if (lane == 0)
         bulk_wait_all();
     __syncwarp();        // warp 0 whole again for the .aligned dealloc
-    grid_dep_launch();   // the scan kernel may start launching
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(s->tmem_base, kTmemCols);

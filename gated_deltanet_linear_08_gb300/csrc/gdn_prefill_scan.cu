@@ -179,6 +179,9 @@ scan_kernel(PrefillArgs p)
     tc_fence_after();
     // launched early behind the prep kernel: its records are read below
     grid_dep_wait();
+    // the output kernel may be scheduled now (its CTAs take the SMs no chain
+    // uses and fetch their z tiles); it waits for this grid's end to read S
+    grid_dep_launch();
     const uint32_t tbase = s->tmem_base;
     const uint32_t idesc = make_idesc_f16(128, kNv, false, true);
 
@@ -372,7 +375,6 @@ scan_kernel(PrefillArgs p)
             set_status(p.status, kStatusRange);
     }
 
-    grid_dep_launch();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {

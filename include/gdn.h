@@ -125,10 +125,9 @@ gdn_status_t gdn_prefill(const gdn_shape_t *shape,
  * fewer tokens with more sequences) and <= 9 at Hv = 48.  Nothing in the
  * array needs clearing between calls.
  * The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture.  Every
- * call on a device shares the one array, so calls that may overlap on the
- * GPU (on different streams, or from different host threads) race and must
- * be ordered by the caller.  Allocates nothing.
+ * device current).  Every call on a device shares the one array, so calls
+ * that may overlap on the GPU (on different streams, or from different host
+ * threads) race and must be ordered by the caller.  Allocates nothing.
  */
 gdn_status_t gdn_prefill_noalloc(const gdn_shape_t *shape,
                                  const void *q, const void *k, const void *v,
