@@ -120,12 +120,52 @@ __device__ __forceinline__ void conv_store4(const DecodeArgs &p, int slot, int c
     }
 }
 
+constexpr int kMaxTokens = 8;   // tokens per sequence in one call
+constexpr int kMaxDevices = 64;
+
+// L2 prefetch of the 128-byte lines of one 256-byte token row, by two lanes.
+__device__ __forceinline__ void prefetch_row_l2(const void *row, int half)
+{
+    asm volatile("prefetch.global.L2 [%0];" :: "l"(reinterpret_cast<const char *>(row) + half * 128));
+}
+
+// The state and token rows of the CTA `ahead` places later in launch order
+// (about one wave of resident CTAs later) are prefetched into L2, so that
+// CTA's loads hit L2 while HBM keeps streaming the following wave.  Warp 4
+// (lane 0) prefetches the 64 KB state with one bulk prefetch, warp 5 the
+// token rows.
+__device__ __forceinline__ void draft_prefetch_ahead(const DecodeArgs &p, int ahead, int warp, int lane)
+{
+    const int b = blockIdx.x + blockIdx.y * gridDim.x + ahead;
+    if (ahead <= 0 || b >= gridDim.x * gridDim.y)
+        return;
+    const int h = b % gridDim.x, n = b / gridDim.x;
+    if (warp == 4 && lane == 0) {
+        const int slot = p.state_idx ? p.state_idx[n] : n;
+        if (slot >= 0 && slot < p.num_slots) {
+            const float *S = p.state + ((size_t)slot * p.hv + h) * (size_t)(kD * kD);
+            bulk_prefetch_l2(S, (uint32_t)(kD * kD * sizeof(float)));
+        }
+    } else if (warp == 5 && lane < 2 * kMaxTokens) {
+        const int t = lane >> 1, half = lane & 1;
+        if (t < p.tokens) {
+            const int64_t tok = (int64_t)n * p.tokens + t;
+            const int hq = h / (p.hv / p.hk);
+            prefetch_row_l2(reinterpret_cast<const __nv_bfloat16 *>(p.k) + tok * p.in.k.t + (int64_t)hq * p.in.k.h, half);
+            prefetch_row_l2(reinterpret_cast<const __nv_bfloat16 *>(p.q) + tok * p.in.q.t + (int64_t)hq * p.in.q.h, half);
+            prefetch_row_l2(reinterpret_cast<const __nv_bfloat16 *>(p.v) + tok * p.in.v.t + (int64_t)h * p.in.v.h, half);
+            if (p.z)
+                prefetch_row_l2(reinterpret_cast<const __nv_bfloat16 *>(p.z) + tok * p.in.z.t + (int64_t)h * p.in.z.h, half);
+        }
+    }
+}
+
 // KW: width of the causal conv ahead of the core (0: none).  Warps 0-2 keep,
 // per lane, the conv weights and the K-1 previous raw inputs of their four
 // k, q or v channels in registers across the tokens.
 template <bool kNorm, int KW>
 __global__ void __launch_bounds__(kThreads, 2)
-decode_kernel(DecodeArgs p)
+decode_kernel(DecodeArgs p, int ahead)
 {
     const int h = blockIdx.x, n = blockIdx.y;
     const int hv = p.hv, hk = p.hk, T = p.tokens;
@@ -184,6 +224,8 @@ decode_kernel(DecodeArgs p)
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 s_v[lane * 4 + j] = f[j];
+        } else if (warp >= 4 && t == 0) {
+            draft_prefetch_ahead(p, ahead, warp, lane);
         } else if (warp == 3 && lane == 0) {
             const float av = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.a)[(int64_t)tok * p.in.a.t + (int64_t)h * p.in.a.h]);
             const float bv = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.b)[(int64_t)tok * p.in.b.t + (int64_t)h * p.in.b.h]);
@@ -296,7 +338,6 @@ decode_kernel(DecodeArgs p)
 // in the single-token kernel, with the same thread layout (warp w: rows
 // w + 8i; lane: four columns).
 constexpr int kMaxDraft = 8;
-constexpr int kMaxDevices = 64;
 constexpr int kDotWarps = 4;   // warps 4-7 form the dot products under the input loads
 
 struct DraftSmem {
@@ -371,43 +412,6 @@ __device__ __forceinline__ void draft_partials(const float4 (&st)[kRowsPerThread
 __host__ __device__ constexpr size_t draft_part_bytes(int T)
 {
     return (size_t)2 * T * kWarps * kD * sizeof(float);
-}
-
-// L2 prefetch of the 128-byte lines of one 256-byte token row, by two lanes.
-__device__ __forceinline__ void prefetch_row_l2(const void *row, int half)
-{
-    asm volatile("prefetch.global.L2 [%0];" :: "l"(reinterpret_cast<const char *>(row) + half * 128));
-}
-
-// The state and token rows of the CTA `ahead` places later in launch order
-// (about one wave of resident CTAs later) are prefetched into L2, so that
-// CTA's loads hit L2 while HBM keeps streaming the following wave.  Warp 4
-// (lane 0) prefetches the 64 KB state with one bulk prefetch, warp 5 the
-// token rows.
-__device__ __forceinline__ void draft_prefetch_ahead(const DecodeArgs &p, int ahead, int warp, int lane)
-{
-    const int b = blockIdx.x + blockIdx.y * gridDim.x + ahead;
-    if (ahead <= 0 || b >= gridDim.x * gridDim.y)
-        return;
-    const int h = b % gridDim.x, n = b / gridDim.x;
-    if (warp == 4 && lane == 0) {
-        const int slot = p.state_idx ? p.state_idx[n] : n;
-        if (slot >= 0 && slot < p.num_slots) {
-            const float *S = p.state + ((size_t)slot * p.hv + h) * (size_t)(kD * kD);
-            bulk_prefetch_l2(S, (uint32_t)(kD * kD * sizeof(float)));
-        }
-    } else if (warp == 5 && lane < 2 * kMaxDraft) {
-        const int t = lane >> 1, half = lane & 1;
-        if (t < p.tokens) {
-            const int64_t tok = (int64_t)n * p.tokens + t;
-            const int hq = h / (p.hv / p.hk);
-            prefetch_row_l2(reinterpret_cast<const __nv_bfloat16 *>(p.k) + tok * p.in.k.t + (int64_t)hq * p.in.k.h, half);
-            prefetch_row_l2(reinterpret_cast<const __nv_bfloat16 *>(p.q) + tok * p.in.q.t + (int64_t)hq * p.in.q.h, half);
-            prefetch_row_l2(reinterpret_cast<const __nv_bfloat16 *>(p.v) + tok * p.in.v.t + (int64_t)h * p.in.v.h, half);
-            if (p.z)
-                prefetch_row_l2(reinterpret_cast<const __nv_bfloat16 *>(p.z) + tok * p.in.z.t + (int64_t)h * p.in.z.h, half);
-        }
-    }
 }
 
 template <bool kNorm, int KW>
@@ -663,15 +667,52 @@ conv_roll_kernel(DecodeArgs p)
     conv_roll8(p.conv, p.q, p.k, p.v, p.in, p.hk, c, slot, slot, (int64_t)n * p.tokens, p.tokens);
 }
 
+// CTAs of `kernel` resident on the current device at once (the distance of
+// the one-wave-ahead L2 prefetch), computed once per device and kernel.
+template <typename Kernel>
+cudaError_t resident_ctas(Kernel kernel, size_t smem, std::atomic<int> (&cache)[kMaxDevices], int &out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    out = cache[dev].load(std::memory_order_relaxed);
+    if (!out) {
+        int sms = 0, per_sm = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem);
+        if (e != cudaSuccess)
+            return e;
+        out = sms * (per_sm > 0 ? per_sm : 1);
+        cache[dev].store(out, std::memory_order_relaxed);
+    }
+    return cudaSuccess;
+}
+
+template <bool kNorm, int KW>
+cudaError_t launch_one(const DecodeArgs &args, dim3 grid, cudaStream_t stream)
+{
+    static std::atomic<int> resident[kMaxDevices];
+    int ahead = 0;
+    cudaError_t e = resident_ctas(decode_kernel<kNorm, KW>, 0, resident, ahead);
+    if (e != cudaSuccess)
+        return e;
+    decode_kernel<kNorm, KW><<<grid, kThreads, 0, stream>>>(args, ahead);
+    return cudaGetLastError();
+}
+
 template <bool kNorm>
-void launch_width(const DecodeArgs &args, dim3 grid, cudaStream_t stream)
+cudaError_t launch_width(const DecodeArgs &args, dim3 grid, cudaStream_t stream)
 {
     switch (args.conv.width) {
-    case 1: decode_kernel<kNorm, 1><<<grid, kThreads, 0, stream>>>(args); break;
-    case 2: decode_kernel<kNorm, 2><<<grid, kThreads, 0, stream>>>(args); break;
-    case 3: decode_kernel<kNorm, 3><<<grid, kThreads, 0, stream>>>(args); break;
-    case 4: decode_kernel<kNorm, 4><<<grid, kThreads, 0, stream>>>(args); break;
-    default: decode_kernel<kNorm, 0><<<grid, kThreads, 0, stream>>>(args);
+    case 1: return launch_one<kNorm, 1>(args, grid, stream);
+    case 2: return launch_one<kNorm, 2>(args, grid, stream);
+    case 3: return launch_one<kNorm, 3>(args, grid, stream);
+    case 4: return launch_one<kNorm, 4>(args, grid, stream);
+    default: return launch_one<kNorm, 0>(args, grid, stream);
     }
 }
 
@@ -679,33 +720,17 @@ template <bool kNorm, int KW>
 cudaError_t launch_draft_width(const DecodeArgs &args, dim3 grid, cudaStream_t stream)
 {
     // the partial sums of the longest draft exceed the default dynamic
-    // shared-memory limit; the attribute is set once per kernel, and the
-    // prefetch distance (the CTAs resident at once) once per device
+    // shared-memory limit; the attribute is set once per kernel
     static const cudaError_t attr = cudaFuncSetAttribute(
         decode_draft_kernel<kNorm, KW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)draft_part_bytes(kMaxDraft));
     if (attr != cudaSuccess)
         return attr;
     static std::atomic<int> resident[kMaxDevices];
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    int ahead = 0;   // sized for the longest draft: the fewest CTAs resident
+    cudaError_t e = resident_ctas(decode_draft_kernel<kNorm, KW>, draft_part_bytes(kMaxDraft), resident, ahead);
     if (e != cudaSuccess)
         return e;
-    if (dev < 0 || dev >= kMaxDevices)
-        return cudaErrorInvalidDevice;
-    const size_t smem = draft_part_bytes(args.tokens);
-    int ahead = resident[dev].load(std::memory_order_relaxed);
-    if (!ahead) {
-        int sms = 0, per_sm = 0;
-        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e == cudaSuccess)   // sized for the longest draft: the fewest CTAs resident
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_draft_kernel<kNorm, KW>, kThreads,
-                                                              draft_part_bytes(kMaxDraft));
-        if (e != cudaSuccess)
-            return e;
-        ahead = sms * (per_sm > 0 ? per_sm : 1);
-        resident[dev].store(ahead, std::memory_order_relaxed);
-    }
-    decode_draft_kernel<kNorm, KW><<<grid, kThreads, smem, stream>>>(args, ahead);
+    decode_draft_kernel<kNorm, KW><<<grid, kThreads, draft_part_bytes(args.tokens), stream>>>(args, ahead);
     return cudaGetLastError();
 }
 
@@ -732,11 +757,7 @@ cudaError_t launch_decode(const DecodeArgs &args, cudaStream_t stream)
     if (args.tokens > 1) {
         e = args.z ? launch_draft<true>(args, grid, stream) : launch_draft<false>(args, grid, stream);
     } else {
-        if (args.z)
-            launch_width<true>(args, grid, stream);
-        else
-            launch_width<false>(args, grid, stream);
-        e = cudaGetLastError();
+        e = args.z ? launch_width<true>(args, grid, stream) : launch_width<false>(args, grid, stream);
     }
     if (e != cudaSuccess || args.conv.width <= 1 || !args.conv.state_out || args.conv.state_out != args.conv.state_in)
         return e;
