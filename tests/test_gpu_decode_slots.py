@@ -11,7 +11,7 @@ import torch
 import oracle
 from gated_deltanet_linear_08_gb300.inputs import (DecodeCase, DecodeSlotsCase, make_decode_inputs,
                                                    make_decode_slots_inputs, to_f64)
-from parity_util import DECODE_STATE_REL, assert_out_close
+from parity_util import DECODE_STATE_REL, assert_out_close, record
 
 pytestmark = pytest.mark.gpu
 
@@ -42,9 +42,11 @@ def _run(case):
                                        to_f64(x["A_log"]), to_f64(x["dt_bias"]), S,
                                        z=None if x["z"] is None else to_f64(x["z"])[live, t],
                                        norm_w=to_f64(x["norm_w"]), eps=x["eps"])
-    assert_out_close(got_out[live], ref, "decode_slots out")
+    assert_out_close(got_out[live], ref, f"{case.name} out")
     Sg = got_pool[torch.as_tensor(idx[live].astype(np.int64))].double().numpy()
     rel = np.abs(Sg - S).max() / np.abs(S).max()
+    record(f"{case.name} state", "state", dict(max_abs=float(rel), violations=int(rel > DECODE_STATE_REL)),
+           f"max|dS|/max|S| <= {DECODE_STATE_REL:g}")
     assert rel <= DECODE_STATE_REL, rel
     # skipped sequences: zero outputs; slots nobody named: bitwise untouched
     assert np.all(got_out[dead] == 0)
@@ -58,7 +60,7 @@ def _run(case):
 @pytest.mark.parametrize("tokens", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("gated", [False, True])
 def test_decode_slots_multi_token(tokens, gated):
-    _run(DecodeSlotsCase(f"slots_T{tokens}", batch=64, tokens=tokens, slots=96, skipped=5,
+    _run(DecodeSlotsCase(f"slots_T{tokens}{'_gnorm' if gated else ''}", batch=64, tokens=tokens, slots=96, skipped=5,
                          gated_norm=gated, seed=tokens))
 
 
