@@ -6,15 +6,18 @@
 //
 // One CTA per (sequence, value head) streams its 128x128 fp32 state (64 KB)
 // exactly once: every thread keeps 16 rows x 4 columns of the state in
-// registers from the read, through every token, to the write.  Per token
+// registers from the read to the write.  For one token
 //   r_k = S_old^T kn,  r_q = S_old^T qn          (reductions over Dk)
 //   delta = beta (v - e^g r_k)
 //   o = scale (e^g r_q + (kn . qn) delta)        (= scale * S_new^T qn)
 //   S_new = e^g S_old + kn delta^T
 // so both reductions come from the old state and the update needs no second
-// pass.  The path is HBM-bound (about 7 flop per 8 bytes of state for one
-// token): loads and stores are 16-byte, warp-contiguous rows of 512 bytes,
-// marked streaming so they do not displace other data in L2.
+// pass (decode_kernel); a draft of 2..8 tokens unrolls the same recurrence
+// over its tokens and still reads the state once (decode_draft_kernel).  The
+// path is HBM-bound (about 7 flop per 8 bytes of state for one token): loads
+// and stores are 16-byte, warp-contiguous rows of 512 bytes, marked streaming
+// so they do not displace other data in L2, and each CTA prefetches into L2
+// the state of the CTA one resident wave after it.
 #include <atomic>
 
 #include "common.cuh"
@@ -160,15 +163,15 @@ __device__ __forceinline__ void draft_prefetch_ahead(const DecodeArgs &p, int ah
     }
 }
 
-// KW: width of the causal conv ahead of the core (0: none).  Warps 0-2 keep,
-// per lane, the conv weights and the K-1 previous raw inputs of their four
-// k, q or v channels in registers across the tokens.
+// One token per sequence.  KW: width of the causal conv ahead of the core
+// (0: none); warps 0-2 keep, per lane, the conv weights and the K-1 previous
+// raw inputs of their four k, q or v channels in registers.
 template <bool kNorm, int KW>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_kernel(DecodeArgs p, int ahead)
 {
     const int h = blockIdx.x, n = blockIdx.y;
-    const int hv = p.hv, hk = p.hk, T = p.tokens;
+    const int hv = p.hv, hk = p.hk;
     const int hq = h / (hv / hk);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -195,8 +198,8 @@ decode_kernel(DecodeArgs p, int ahead)
         conv_load4<KW>(p, slot, conv_channel(warp, lane, hk, hq, h), cw, win);
 
     const float scale = rsqrtf((float)kD);
-    for (int t = 0; t < T; ++t) {
-        const size_t tok = (size_t)n * T + t;
+    {
+        const size_t tok = (size_t)n;   // one token per sequence
         // 2. Per-token inputs: warp 0 normalises k, warp 1 q, warp 2 loads v,
         //    warp 3 computes the gate and beta.
         if (warp < 2) {
@@ -224,7 +227,7 @@ decode_kernel(DecodeArgs p, int ahead)
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 s_v[lane * 4 + j] = f[j];
-        } else if (warp >= 4 && t == 0) {
+        } else if (warp >= 4) {
             draft_prefetch_ahead(p, ahead, warp, lane);
         } else if (warp == 3 && lane == 0) {
             const float av = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.a)[(int64_t)tok * p.in.a.t + (int64_t)h * p.in.a.h]);
@@ -307,8 +310,6 @@ decode_kernel(DecodeArgs p, int ahead)
             st[i].z = fmaf(eg, st[i].z, kk * d4.z);
             st[i].w = fmaf(eg, st[i].w, kk * d4.w);
         }
-        if (t + 1 < T)
-            __syncthreads();   // the next token overwrites the shared inputs
     }
 
     // 6. Written back in place, once.
