@@ -17,16 +17,15 @@ namespace {
 // Status word the kernels OR bits into when a bounded wait runs out.
 __device__ uint32_t g_device_status;
 
-constexpr int kMaxDevices = 64;
 // Device address of g_device_status, per device.  Host threads may make their
 // first call on a device at the same time: each then looks the address up and
 // stores the same value, which the atomic makes a well-defined race.
-std::atomic<uint32_t *> g_status_ptr[kMaxDevices];
+std::atomic<uint32_t *> g_status_ptr[gdn::kMaxDevices];
 
 uint32_t *status_ptr()
 {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= gdn::kMaxDevices)
         return nullptr;
     uint32_t *cached = g_status_ptr[dev].load(std::memory_order_relaxed);
     if (!cached) {

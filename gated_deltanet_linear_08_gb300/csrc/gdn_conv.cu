@@ -28,7 +28,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kRun = 8;   // tokens per thread
 constexpr int kCh = 4;    // channels per thread (one 8-byte vector)
-constexpr int kMaxDevices = 64;
 
 // Sequence holding token t: the last n with cu[n] <= t (cu nondecreasing in
 // a well-formed call; otherwise any n in range, which only ever reads

@@ -124,7 +124,6 @@ __device__ __forceinline__ void conv_store4(const DecodeArgs &p, int slot, int c
 }
 
 constexpr int kMaxTokens = 8;   // tokens per sequence in one call
-constexpr int kMaxDevices = 64;
 
 // L2 prefetch of the 128-byte lines of one 256-byte token row, by two lanes.
 __device__ __forceinline__ void prefetch_row_l2(const void *row, int half)
@@ -137,7 +136,7 @@ __device__ __forceinline__ void prefetch_row_l2(const void *row, int half)
 // CTA's loads hit L2 while HBM keeps streaming the following wave.  Warp 4
 // (lane 0) prefetches the 64 KB state with one bulk prefetch, warp 5 the
 // token rows.
-__device__ __forceinline__ void draft_prefetch_ahead(const DecodeArgs &p, int ahead, int warp, int lane)
+__device__ __forceinline__ void prefetch_ahead_l2(const DecodeArgs &p, int ahead, int warp, int lane)
 {
     const int b = blockIdx.x + blockIdx.y * gridDim.x + ahead;
     if (ahead <= 0 || b >= gridDim.x * gridDim.y)
@@ -228,7 +227,7 @@ decode_kernel(DecodeArgs p, int ahead)
             for (int j = 0; j < 4; ++j)
                 s_v[lane * 4 + j] = f[j];
         } else if (warp >= 4) {
-            draft_prefetch_ahead(p, ahead, warp, lane);
+            prefetch_ahead_l2(p, ahead, warp, lane);
         } else if (warp == 3 && lane == 0) {
             const float av = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.a)[(int64_t)tok * p.in.a.t + (int64_t)h * p.in.a.h]);
             const float bv = bf2f(reinterpret_cast<const __nv_bfloat16 *>(p.b)[(int64_t)tok * p.in.b.t + (int64_t)h * p.in.b.h]);
@@ -509,7 +508,7 @@ decode_draft_kernel(DecodeArgs p, int ahead)
             sm.gam[lane] = expf(g);
         }
     } else {
-        draft_prefetch_ahead(p, ahead, warp, lane);
+        prefetch_ahead_l2(p, ahead, warp, lane);
         if (kNorm) {
             const int c = tid - 4 * 32;
             for (int t = 0; t < T; ++t)
@@ -721,11 +720,20 @@ template <bool kNorm, int KW>
 cudaError_t launch_draft_width(const DecodeArgs &args, dim3 grid, cudaStream_t stream)
 {
     // the partial sums of the longest draft exceed the default dynamic
-    // shared-memory limit; the attribute is set once per kernel
-    static const cudaError_t attr = cudaFuncSetAttribute(
-        decode_draft_kernel<kNorm, KW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)draft_part_bytes(kMaxDraft));
-    if (attr != cudaSuccess)
-        return attr;
+    // shared-memory limit: the attribute is set with the first launch on a
+    // device, before the occupancy query (a racing repeat sets the same value)
+    static std::atomic<bool> configured[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    if (!configured[dev].load(std::memory_order_relaxed)) {
+        const cudaError_t attr = cudaFuncSetAttribute(decode_draft_kernel<kNorm, KW>,
+                                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                      (int)draft_part_bytes(kMaxDraft));
+        if (attr != cudaSuccess)
+            return attr;
+        configured[dev].store(true, std::memory_order_relaxed);
+    }
     static std::atomic<int> resident[kMaxDevices];
     int ahead = 0;   // sized for the longest draft: the fewest CTAs resident
     cudaError_t e = resident_ctas(decode_draft_kernel<kNorm, KW>, draft_part_bytes(kMaxDraft), resident, ahead);

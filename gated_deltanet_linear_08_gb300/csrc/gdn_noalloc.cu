@@ -27,11 +27,10 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes + 1024];
 
-constexpr int kMaxDevices = 64;
 // Device address of g_noalloc_scratch, per device.  Two host threads making
 // their first call on one device at the same time both look it up and store
 // the same value; the atomic keeps that race well defined.
-std::atomic<void *> g_scratch_ptr[kMaxDevices];
+std::atomic<void *> g_scratch_ptr[gdn::kMaxDevices];
 
 }  // namespace
 
@@ -46,7 +45,7 @@ extern "C" gdn_status_t gdn_prefill_noalloc(const gdn_shape_t *s, const void *q,
     if (need > kNoAllocScratchBytes)
         return GDN_ERR_WORKSPACE;   // the problem is larger than the built-in scratch
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= gdn::kMaxDevices)
         return GDN_ERR_CUDA;
     void *ptr = g_scratch_ptr[dev].load(std::memory_order_relaxed);
     if (!ptr) {

@@ -37,6 +37,8 @@
 // The CTA's unit list (first token and rows of each unit) and the norm
 // weights are read before the dependency wait too: cu_seqlens and the weights
 // are call inputs, and the chunk index is final before the scan starts.
+#include <atomic>
+
 #include "chunks.cuh"
 #include "common.cuh"
 #include "kernels.h"
@@ -364,14 +366,22 @@ out_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_z, const __grid
 
 cudaError_t launch_prefill_out(const PrefillArgs &p, cudaStream_t stream)
 {
-    static bool configured = false;
-    if (!configured) {
+    // the shared-memory attribute and the SM count, once per device (a repeat
+    // from a racing host thread stores the same values)
+    static std::atomic<int> sm_count[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    int sms = sm_count[dev].load(std::memory_order_relaxed);
+    if (!sms) {
         cudaError_t e = cudaFuncSetAttribute(out_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(out_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess)
             return e;
-        configured = true;
+        sm_count[dev].store(sms, std::memory_order_relaxed);
     }
     CUtensorMap tz, to;
     if (!encode_tile_map(&to, p.out, p.hv, p.total_tokens, (int64_t)p.hv * kD, kD))
@@ -382,18 +392,9 @@ cudaError_t launch_prefill_out(const PrefillArgs &p, cudaStream_t stream)
     } else {
         tz = to;   // unused without the epilogue
     }
-    static int sm_count[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
-        return cudaErrorInvalidDevice;
-    if (!sm_count[dev]) {
-        cudaError_t e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess)
-            return e;
-    }
     const int units = p.max_chunks * p.hv;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(units < sm_count[dev] ? units : sm_count[dev]);
+    cfg.gridDim = dim3(units < sms ? units : sms);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;

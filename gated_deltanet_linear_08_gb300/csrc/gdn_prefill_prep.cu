@@ -35,6 +35,8 @@
 // The chunk's q, k and v tiles arrive by tensor-map copies issued at entry:
 // k and q land directly in the 128-byte-swizzled layout the first tcgen05
 // product reads, so no thread waits on a global load.
+#include <atomic>
+
 #include <cuda.h>
 
 #include "chunks.cuh"
@@ -799,12 +801,17 @@ cudaError_t launch_chunk_index(const PrefillArgs &p, cudaStream_t stream)
 
 cudaError_t launch_prefill_prep(const PrefillArgs &p, cudaStream_t stream)
 {
-    static bool configured = false;   // attribute is per function, process-wide
-    if (!configured) {
+    // the shared-memory attribute, once per device (a repeat from a racing
+    // host thread sets the same value)
+    static std::atomic<bool> configured[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    if (!configured[dev].load(std::memory_order_relaxed)) {
         cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess)
             return e;
-        configured = true;
+        configured[dev].store(true, std::memory_order_relaxed);
     }
     CUtensorMap tq, tk, tv;
     if (!encode_tile_map(&tq, p.q, p.hk, p.total_tokens, p.in.q.t, p.in.q.h)

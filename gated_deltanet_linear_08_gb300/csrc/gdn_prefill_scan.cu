@@ -35,6 +35,8 @@
 // One CTA per SM with four stages (copies run well ahead of the chain); with
 // more chains than CTAs, each CTA runs its share in turn, the next chain's
 // initial state loaded while the current one runs.
+#include <atomic>
+
 #include "chunks.cuh"
 #include "common.cuh"
 #include "conv.cuh"
@@ -411,14 +413,15 @@ namespace {
 template <int NS>
 cudaError_t resident_ctas(int &out)
 {
-    static int cache[64] = {};
+    static std::atomic<int> cache[kMaxDevices];   // a racing repeat stores the same value
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    if (dev < 0 || dev >= 64)
+    if (dev < 0 || dev >= kMaxDevices)
         return cudaErrorInvalidDevice;
-    if (!cache[dev]) {
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (!n) {
         e = cudaFuncSetAttribute(scan_kernel<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)ScanCfg<NS>::kSmemBytes);
         int sms = 0, per_sm = 0;
@@ -429,9 +432,10 @@ cudaError_t resident_ctas(int &out)
                                                               ScanCfg<NS>::kSmemBytes);
         if (e != cudaSuccess)
             return e;
-        cache[dev] = sms * (per_sm > 0 ? per_sm : 1);
+        n = sms * (per_sm > 0 ? per_sm : 1);
+        cache[dev].store(n, std::memory_order_relaxed);
     }
-    out = cache[dev];
+    out = n;
     return cudaSuccess;
 }
 }  // namespace

@@ -10,6 +10,10 @@
 
 namespace gdn {
 
+// Devices one process may drive: the size of the per-device caches (device
+// addresses, resident CTA counts).
+constexpr int kMaxDevices = 64;
+
 // Element strides of one token input: between consecutive tokens and
 // between consecutive heads (rows of 128 elements for q, k, v, z; one element
 // for a, b).
