@@ -194,7 +194,23 @@ out_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_z, const __grid
         }
         __syncwarp();
     } else {
-        // launched early behind the scan kernel: its S copies are read below
+        // Launched early behind the scan kernel, whose S records are read
+        // below.  The prep kernel's part of the first two runs ([Qc | Fc | V],
+        // 40 KB of 72) is requested before the dependency wait: prep finished
+        // before the scan passed its own wait, and this grid launches after
+        // that.  Only the S part waits.
+        constexpr uint32_t kPrepPart = (uint32_t)(kWsS - kWsQc0);
+        int early = 0;   // runs whose prep part is in flight (loader lane)
+        if (warp == kLoadWarp && lane == 0) {
+            for (; early < kRunStages && early < nj; ++early) {
+                int h, tok0, L;
+                if (!unit_at(early, h, tok0, L))
+                    break;
+                const unsigned char *rec = p.workspace + (size_t)((int)blockIdx.x + early * (int)gridDim.x) * kPerVHead;
+                mbar_arrive_expect_tx(&s->full[early], kRunBytes);
+                bulk_g2s(sm + early * kRunBytes, rec + kWsQc0, kPrepPart, &s->full[early]);
+            }
+        }
         grid_dep_wait();
         if (warp == kLoadWarp) {
             if (lane == 0) {
@@ -210,10 +226,14 @@ out_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_z, const __grid
                         break;
                     unsigned char *stage = sm + rs * kRunBytes;
                     const unsigned char *rec = p.workspace + (size_t)((int)blockIdx.x + j * (int)gridDim.x) * kPerVHead;
-                    mbar_arrive_expect_tx(&s->full[rs], kRunBytes);
+                    if (j < early) {   // the S part of a run whose prep part is on its way
+                        bulk_g2s(stage + kPrepPart, rec + kWsS, kRunBytes - kPrepPart, &s->full[rs]);
+                    } else {
+                        mbar_arrive_expect_tx(&s->full[rs], kRunBytes);
 #pragma unroll
-                    for (int q = 0; q < 3; ++q)
-                        bulk_g2s(stage + q * 24576, rec + kWsQc0 + q * 24576, 24576, &s->full[rs]);
+                        for (int q = 0; q < 3; ++q)
+                            bulk_g2s(stage + q * 24576, rec + kWsQc0 + q * 24576, 24576, &s->full[rs]);
+                    }
                     ++issued[rs];
                 }
                 if (*reinterpret_cast<volatile int *>(&s->fail)) {
