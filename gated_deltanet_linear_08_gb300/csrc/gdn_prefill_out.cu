@@ -36,7 +36,10 @@
 //             epilogue four units before
 // The CTA's unit list (first token and rows of each unit) and the norm
 // weights are read before the dependency wait too: cu_seqlens and the weights
-// are call inputs, and the chunk index is final before the scan starts.
+// are call inputs, and the chunk index is final before the scan starts.  So is
+// the prep kernel's part of the first two record runs ([Qc | Fc | V]): prep
+// finished before the scan passed its own wait, and this grid launches only
+// after that; the S part of those runs waits.
 #include <atomic>
 
 #include "chunks.cuh"

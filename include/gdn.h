@@ -166,8 +166,10 @@ gdn_status_t gdn_decode(const gdn_shape_t *shape,
  * against a pool of recurrent-state slots (SGLang page "[Perf] Pack the
  * Qwen3.5 GDN input projection on CUDA", Accuracy Tests: mamba slots).
  * Each sequence's state is read once, advanced through its tokens in order
- * exactly as the recurrence of gdn_decode would advance it token by token,
- * and written back once, in place.
+ * by the recurrence of gdn_decode, and written back once, in place.  A draft
+ * of 2..8 tokens is solved together in that one pass (the recurrence
+ * unrolled over the draft), which gives the token-by-token values up to
+ * fp32 rounding; one token is exactly gdn_decode.
  *
  *   shape->num_seqs = B; shape->total_tokens must equal B * tokens.
  *   q, k     bf16 [B, tokens, Hk, 128];  v bf16 [B, tokens, Hv, 128]
