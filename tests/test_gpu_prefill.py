@@ -5,8 +5,9 @@ T=2048 with the gated-RMSNorm epilogue, also as 2x1024 with the state
 carried; 16 varlen sequences at Hv=48), the chunk boundaries the pegainfer
 page tests ("feat(qwen35): add SM120 FlashInfer GDN prefill candidate",
 Correctness: T = 1, 2, 63, 64, 65, 127, 128; chunked vs unchunked prefill),
-grouped heads, empty sequences, in-place state, weak and pure decay, and
-run-to-run determinism.
+grouped heads, empty sequences, in-place state, weak and pure decay, long
+sequences (16,384 tokens; 8,192 with weak decay), and run-to-run
+determinism.
 """
 import math
 
@@ -63,6 +64,20 @@ def test_prefill_in_place_state():
 
 def test_prefill_weak_decay_carries_state():
     _check(PrefillCase("weak", seqlens=[700], hk=2, hv=4, init_state=True, seed=6,
+                       a_log_const=math.log(0.01)), scale_state=True)
+
+
+def test_prefill_long_sequence_16k_tokens():
+    """One 16,384-token sequence (256 chunks per chain, eight times the
+    T = 2048 workload's) with initial states and the gated norm: the scan's
+    stage ring streams a long chain, the output kernel walks ~55 units per CTA."""
+    _check(PrefillCase("T16384_gnorm", seqlens=[16384], init_state=True, gated_norm=True, seed=16))
+
+
+def test_prefill_long_weak_decay_carries_state():
+    """8,192 tokens with weak decay: the state carries across many chunks, so
+    the fp16 operand roundings of 128 chunk steps accumulate in it."""
+    _check(PrefillCase("weak_T8192", seqlens=[8192], hk=2, hv=4, init_state=True, seed=17,
                        a_log_const=math.log(0.01)), scale_state=True)
 
 
