@@ -55,18 +55,23 @@ def test_prefill_in_pieces_with_carried_states_matches_one_call():
     assert gdn.check_device_status() == 0
 
 
-def test_graph_captured_decode_loop_matches_eager():
+@pytest.mark.parametrize("tokens", [1, 4])
+def test_graph_captured_decode_loop_matches_eager(tokens):
+    """A captured loop of slot-pool decode steps replays to the eager results
+    bit for bit: one token per step (the single-token kernel) or a 4-token
+    draft per step (the draft kernel)."""
     import gated_deltanet_linear_08_gb300 as gdn
-    case = DecodeSlotsCase("graph", batch=16, tokens=1, slots=40, skipped=2, hk=4, hv=8, seed=5)
+    case = DecodeSlotsCase("graph", batch=16, tokens=tokens, slots=40, skipped=2, hk=4, hv=8, seed=5)
     steps = 12
-    ys = [make_decode_slots_inputs(DecodeSlotsCase(case.name, batch=case.batch, tokens=1, slots=case.slots,
+    ys = [make_decode_slots_inputs(DecodeSlotsCase(case.name, batch=case.batch, tokens=tokens, slots=case.slots,
                                                    skipped=case.skipped, hk=case.hk, hv=case.hv, seed=100 + s))
           for s in range(steps)]
     base = make_decode_slots_inputs(case)
     toks = [{n: y[n].cuda() for n in ("q", "k", "v", "a", "b")} for y in ys]
     A_log, dt = base["A_log"].cuda(), base["dt_bias"].cuda()
     idx = base["state_idx"].cuda()
-    outs_e = [torch.empty(case.batch, 1, case.hv, 128, dtype=torch.bfloat16, device="cuda") for _ in range(steps)]
+    outs_e = [torch.empty(case.batch, tokens, case.hv, 128, dtype=torch.bfloat16, device="cuda")
+              for _ in range(steps)]
     outs_g = [torch.empty_like(o) for o in outs_e]
 
     def loop(pool, outs, stream=None):
@@ -109,3 +114,40 @@ def test_graph_captured_prefill_matches_eager():
     torch.cuda.synchronize()
     assert torch.equal(out_g, out_e) and torch.equal(fin_g, fin_e)
     assert gdn.check_device_status() == 0
+
+
+_FIRST_CALL_IN_CAPTURE = r"""
+import sys, torch
+sys.path.insert(0, {root!r})
+import gated_deltanet_linear_08_gb300 as gdn
+from gated_deltanet_linear_08_gb300.inputs import DecodeSlotsCase, make_decode_slots_inputs
+x = make_decode_slots_inputs(DecodeSlotsCase("fresh", batch=8, tokens=4, slots=12, skipped=1, hk=2, hv=4, seed=9))
+t = {{n: x[n].cuda() for n in ("q", "k", "v", "a", "b")}}
+A_log, dt, idx = x["A_log"].cuda(), x["dt_bias"].cuda(), x["state_idx"].cuda()
+pool_g, pool_e = x["pool"].cuda(), x["pool"].cuda()
+out_g = torch.empty(8, 4, 4, 128, dtype=torch.bfloat16, device="cuda")
+stream = torch.cuda.Stream()
+graph = torch.cuda.CUDAGraph()
+with torch.cuda.graph(graph, stream=stream):   # the library's first call of this process
+    gdn.decode_slots(t["q"], t["k"], t["v"], t["a"], t["b"], A_log, dt, pool_g, state_idx=idx, out=out_g,
+                     stream=stream)
+graph.replay()
+out_e = gdn.decode_slots(t["q"], t["k"], t["v"], t["a"], t["b"], A_log, dt, pool_e, state_idx=idx)
+torch.cuda.synchronize()
+assert torch.equal(out_g, out_e) and torch.equal(pool_g, pool_e)
+assert gdn.check_device_status() == 0
+print("ok")
+"""
+
+
+def test_first_draft_decode_call_inside_a_capture():
+    """The draft kernel's one-time set-up (its shared-memory attribute and
+    the resident-CTA count) runs inside a stream capture when the capture
+    holds the process's first call; the replay still matches eager."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    res = subprocess.run([sys.executable, "-c", _FIRST_CALL_IN_CAPTURE.format(root=root)],
+                         capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0 and res.stdout.strip().endswith("ok"), res.stdout + res.stderr
