@@ -340,15 +340,16 @@ decode_kernel(DecodeArgs p, int ahead)
 constexpr int kMaxDraft = 8;
 constexpr int kDotWarps = 4;   // warps 4-7 form the dot products under the input loads
 
+template <bool kNorm>
 struct DraftSmem {
     // k_t, q_t normalised, and r_{T-1,s} k_s: permuted so that the 16 rows a
-    // thread of warp w owns (w + 8i) sit contiguous at [w][i]
+    // thread of warp w owns (w + 8i) sit contiguous at [w][i] (the dot
+    // products k_s.k_t and k_s.q_t run over the same permuted order)
     float kp[kMaxDraft][kWarps][kRowsPerThread], qp[kMaxDraft][kWarps][kRowsPerThread];
     float kwp[kMaxDraft][kWarps][kRowsPerThread];
-    float k[kMaxDraft][kD], q[kMaxDraft][kD];   // natural order, for the dot products
     float v[kMaxDraft][kD];                    // v_t; then o_t before the norm
     float dl[kMaxDraft][kD];                   // delta_t
-    float z[kMaxDraft][kD];
+    float z[kNorm ? kMaxDraft : 1][kD];
     float beta[kMaxDraft], gam[kMaxDraft];
     float rat[kMaxDraft][kMaxDraft];           // r_ts, s <= t
     float kk[kMaxDraft][kMaxDraft];            // k_s . k_t, s < t
@@ -370,9 +371,9 @@ __device__ __forceinline__ float2 fma2(float2 x, float2 y, float2 z)
 
 // Per-warp partial sums of NT consecutive tokens from t0:
 // part[2t] = (S0^T k_t) and part[2t+1] = (S0^T q_t) over this warp's rows.
-template <int NT>
+template <int NT, bool kNorm>
 __device__ __forceinline__ void draft_partials(const float4 (&st)[kRowsPerThread], int t0, int warp, int lane,
-                                               const DraftSmem &sm, float *s_part)
+                                               const DraftSmem<kNorm> &sm, float *s_part)
 {
     float2 rk[NT][2], rq[NT][2];
 #pragma unroll
@@ -425,7 +426,7 @@ decode_draft_kernel(DecodeArgs p, int ahead)
 
     extern __shared__ float4 s_dyn[];
     float *s_part = reinterpret_cast<float *>(s_dyn);   // [2T][kWarps][kD]
-    __shared__ __align__(16) DraftSmem sm;
+    __shared__ __align__(16) DraftSmem<kNorm> sm;
 
     const int slot = resolve_slot(p, n, h, tid);
     if (slot < 0)
@@ -455,7 +456,6 @@ decode_draft_kernel(DecodeArgs p, int ahead)
         float cw[KW > 0 ? KW : 1][4], win[KW > 1 ? KW - 1 : 1][4];
         const int chan = conv_channel(warp, lane, hk, hq, h);
         conv_load4<KW>(p, slot, chan, cw, win);
-        float(*dst)[kD] = warp == 0 ? sm.k : warp == 1 ? sm.q : sm.v;
         float(*dstp)[kWarps][kRowsPerThread] = warp == 0 ? sm.kp : sm.qp;
 #pragma unroll
         for (int t = 0; t < kMaxDraft; ++t) {
@@ -475,8 +475,9 @@ decode_draft_kernel(DecodeArgs p, int ahead)
                         const int e = lane * 4 + j;   // row e = (e % 8) + 8 (e / 8)
                         dstp[t][e & 7][e >> 3] = f[j];
                     }
+                } else {
+                    *reinterpret_cast<float4 *>(&sm.v[t][lane * 4]) = make_float4(f[0], f[1], f[2], f[3]);
                 }
-                *reinterpret_cast<float4 *>(&dst[t][lane * 4]) = make_float4(f[0], f[1], f[2], f[3]);
             }
         }
         if (warp < 2)
@@ -520,9 +521,9 @@ decode_draft_kernel(DecodeArgs p, int ahead)
             const int s = pi / T, t = pi - s * T;
             if (s > t)
                 continue;
-            const float4 ks = *reinterpret_cast<const float4 *>(&sm.k[s][lane * 4]);
-            const float4 kt = *reinterpret_cast<const float4 *>(&sm.k[t][lane * 4]);
-            const float4 qt = *reinterpret_cast<const float4 *>(&sm.q[t][lane * 4]);
+            const float4 ks = *reinterpret_cast<const float4 *>(&sm.kp[s][0][0] + lane * 4);
+            const float4 kt = *reinterpret_cast<const float4 *>(&sm.kp[t][0][0] + lane * 4);
+            const float4 qt = *reinterpret_cast<const float4 *>(&sm.qp[t][0][0] + lane * 4);
             float dk = ks.x * kt.x + ks.y * kt.y + ks.z * kt.z + ks.w * kt.w;
             float dq = ks.x * qt.x + ks.y * qt.y + ks.z * qt.z + ks.w * qt.w;
 #pragma unroll
@@ -544,11 +545,11 @@ decode_draft_kernel(DecodeArgs p, int ahead)
     {
         int t0 = 0;
         for (; t0 + 4 <= T; t0 += 4)
-            draft_partials<4>(st, t0, warp, lane, sm, s_part);
+            draft_partials<4, kNorm>(st, t0, warp, lane, sm, s_part);
         switch (T - t0) {
-        case 1: draft_partials<1>(st, t0, warp, lane, sm, s_part); break;
-        case 2: draft_partials<2>(st, t0, warp, lane, sm, s_part); break;
-        case 3: draft_partials<3>(st, t0, warp, lane, sm, s_part); break;
+        case 1: draft_partials<1, kNorm>(st, t0, warp, lane, sm, s_part); break;
+        case 2: draft_partials<2, kNorm>(st, t0, warp, lane, sm, s_part); break;
+        case 3: draft_partials<3, kNorm>(st, t0, warp, lane, sm, s_part); break;
         default: break;
         }
     }
