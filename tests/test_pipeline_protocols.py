@@ -107,7 +107,10 @@ class Sim:
         ones (a thread's tcgen05 commits) complete in issue order."""
         self.asyncs.append((who, ordered, ops))
 
-    def run(self, max_steps=200000):
+    def run(self, max_steps=400000):
+        # some roles run far behind the others (a warp that is rarely
+        # scheduled), so that waits covering long lags are exercised too
+        slow = {name for name in self.roles if self.rng.random() < 0.15}
         for _ in range(max_steps):
             choices = []
             for name, st in self.roles.items():
@@ -139,7 +142,8 @@ class Sim:
                     return
                 raise Violation("deadlock: " + ", ".join(f"{n}: {st[1][:1]}" for n, st in self.roles.items()
                                                           if st[1] != ("done",)))
-            kind, key = self.rng.choice(choices)
+            weights = [0.03 if (k == "role" and n in slow) else 1.0 for k, n in choices]
+            kind, key = self.rng.choices(choices, weights)[0]
             if kind == "async":
                 _, _, ops = self.asyncs.pop(key)
                 for op in ops:
