@@ -10,7 +10,9 @@ graph-captured decode).
     boundaries, so every chunk sees the same tokens and the same fp32 state;
   * a decode loop over a slot pool captured in a CUDA graph and replayed
     equals the same calls made eagerly, bit for bit;
-  * a captured prefill call equals the eager call.
+  * a captured prefill call equals the eager call;
+  * prefill and decode on views into one packed buffer (one host copy per
+    step in a serving loop) equal the calls on separate tensors.
 """
 import numpy as np
 import pytest
@@ -151,3 +153,57 @@ def test_first_draft_decode_call_inside_a_capture():
     res = subprocess.run([sys.executable, "-c", _FIRST_CALL_IN_CAPTURE.format(root=root)],
                          capture_output=True, text=True, timeout=300)
     assert res.returncode == 0 and res.stdout.strip().endswith("ok"), res.stdout + res.stderr
+
+
+def test_calls_on_views_into_one_packed_buffer():
+    """A serving loop that stages a step's inputs in one buffer (one copy
+    per step) calls the library on typed views at 256-byte-aligned offsets
+    of that buffer, and writes its results into views of another.  Prefill
+    (gated norm) and decode through such views equal the same calls on
+    separate tensors bit for bit."""
+    import gated_deltanet_linear_08_gb300 as gdn
+    from gated_deltanet_linear_08_gb300.inputs import DecodeCase, make_decode_inputs
+
+    def pack(tensors):
+        offs, n = [], 0
+        for t in tensors:
+            n = (n + 255) // 256 * 256
+            offs.append(n)
+            n += t.numel() * t.element_size()
+        buf = torch.zeros((n + 255) // 256 * 256, dtype=torch.uint8, device="cuda")
+        views = []
+        for t, o in zip(tensors, offs):
+            v = buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+            v.copy_(t)
+            views.append(v)
+        return buf, views
+
+    x = make_prefill_inputs(PrefillCase("views", seqlens=[300, 77], hk=4, hv=8, init_state=True,
+                                        gated_norm=True, seed=33))
+    d = to_dev(x)
+    keys = ("q", "k", "v", "a", "b", "z")
+    _, pv = pack([d[k] for k in keys])
+    p = dict(zip(keys, pv))
+    T, hv, N = d["q"].shape[0], x["hv"], len(x["seqlens"])
+    _, (out_v, fin_v) = pack([torch.zeros(T, hv, 128, dtype=torch.bfloat16, device="cuda"),
+                              torch.zeros(N, hv, 128, 128, dtype=torch.float32, device="cuda")])
+    gdn.prefill(p["q"], p["k"], p["v"], p["a"], p["b"], d["A_log"], d["dt_bias"], d["cu_seqlens"],
+                init_state=d["init_state"], z=p["z"], norm_w=d["norm_w"], eps=x["eps"],
+                out=out_v, final_state=fin_v)
+    ref_out, ref_fin = gdn.prefill(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"],
+                                   d["cu_seqlens"], init_state=d["init_state"], z=d["z"],
+                                   norm_w=d["norm_w"], eps=x["eps"])
+    torch.cuda.synchronize()
+    assert torch.equal(out_v, ref_out) and torch.equal(fin_v, ref_fin)
+
+    y = make_decode_inputs(DecodeCase("views_dec", batch=24, hk=4, hv=8, steps=1, seed=34))
+    st = {k: t.cuda() for k, t in y["steps"][0].items()}
+    dkeys = ("q", "k", "v", "a", "b")
+    _, dv = pack([st[k] for k in dkeys])
+    s_views, s_ref = y["state"].cuda(), y["state"].cuda()
+    A, dt = y["A_log"].cuda(), y["dt_bias"].cuda()
+    o_v = gdn.decode(*dv, A, dt, s_views)
+    o_r = gdn.decode(*(st[k] for k in dkeys), A, dt, s_ref)
+    torch.cuda.synchronize()
+    assert torch.equal(o_v, o_r) and torch.equal(s_views, s_ref)
+    assert gdn.check_device_status() == 0
