@@ -181,6 +181,9 @@ __device__ void merge_block(unsigned char *sm, const Small *s, int a, int b, int
 
 
 
+// kSingle: the call's single-chunk form (see below); a separate kernel, so
+// that the general form is the code it would be without it.
+template <bool kSingle>
 __global__ void __launch_bounds__(kThreads, 2)
 prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v)
@@ -197,8 +200,28 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
     const bool live = find_chunk(p, gc, seq, tok0, L, bad);
     if (bad && gc == 0 && h == 0 && tid == 0)
         set_status(p.status, kStatusBadSeqlens);
-    if (!live)
+    if (!live) {
+        // single-chunk call: the last chunk index never exists, and its CTA
+        // of head h writes the zero final state of every empty (or
+        // malformed) sequence for h, which no chunk covers
+        if (kSingle && gc == p.max_chunks - 1) {
+            for (int n = 0; n < p.num_seqs; ++n) {
+                const int s0 = p.cu_seqlens[n], e0 = p.cu_seqlens[n + 1];
+                if (seq_ok(p, s0, e0) && e0 > s0)
+                    continue;
+                float4 *dst = reinterpret_cast<float4 *>(p.final_state + ((size_t)n * hv + h) * kD * kD);
+                for (int e = tid; e < kD * kD / 4; e += kThreads)
+                    dst[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
         return;
+    }
+    // single-chunk call (every sequence within one chunk, zero initial
+    // state): the state entering the chunk is zero, so this CTA finishes it:
+    // final state S1 = Bc (as the scan would add it, through fp16) and
+    // outputs o = scale Fc V (the output kernel's Qc S0 term is zero); no
+    // record is written and the scan and output kernels do not run
+    constexpr bool single = kSingle;
     // The scan kernel may be scheduled as soon as every prep CTA has started:
     // its CTAs take SMs that prep's last wave leaves free and run their
     // prologue there; griddepcontrol.wait still holds them until this whole
@@ -261,7 +284,7 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
     __syncthreads();
     if (tid < 64)
         s->eps[tid] = (tid < L) ? exp2f(s->G2[63] - s->G2[tid]) : 0.f;
-    if (tid == 0)
+    if (tid == 0 && !single)
         *reinterpret_cast<float4 *>(ws + kWsScal) = make_float4(exp2f(s->G2[63]), 0.f, 0.f, 0.f);
     wait_bar(s, &s->mbar_tma, 0, p.status);
 
@@ -353,7 +376,7 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
     }
     fence_async_smem();
     __syncthreads();   // the v tile is consumed before [I; P] overwrites it
-    if (tid == 0)
+    if (tid == 0 && !single)
         bulk_s2g(ws + kWsV, sm + kOffStV, (uint32_t)kVBytes);
     __syncwarp();   // warp 0 whole again before the .aligned TMEM loads
 
@@ -507,7 +530,7 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
     tc_fence_before();
     __syncthreads();
 
-    if (tid == 0)
+    if (tid == 0 && !single)
         bulk_s2g(ws + kWsFc, sm + kOffStFc, 8192);
     __syncwarp();
     // ---- 8. Ec = Kn^T BE (TMEM [0,64); A = Kn read MN-major: dk halves 16 KB
@@ -553,7 +576,7 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
     float wr[2][32];
     tmem_ld32x2(s->tmem_base + ((uint32_t)(32 * q) << 16) + 128 + ch * 64,
                 s->tmem_base + ((uint32_t)(32 * q) << 16) + 128 + ch * 64 + 32, wr[0], wr[1]);
-    if (q < 2) {
+    if (q < 2 && !single) {
         const float ei = s->eps[i];
 #pragma unroll
         for (int g = 0; g < 2; ++g)
@@ -586,10 +609,20 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
         if (lane == 0) {
             constexpr uint32_t idesc = make_idesc_f16(128, 128, true, true);
             constexpr uint32_t idesc_b = make_idesc_f16(128, 128, false, true);
+            if (!single) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_f16(s->tmem_base, make_desc(sbase + kOffKQ + kk * 2048, 16384, 1024, kSw128),
-                        make_desc(sbase + kOffBM + kk * 2048, 8192, 1024, kSw128), idesc, kk != 0);
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_f16(s->tmem_base, make_desc(sbase + kOffKQ + kk * 2048, 16384, 1024, kSw128),
+                            make_desc(sbase + kOffBM + kk * 2048, 8192, 1024, kSw128), idesc, kk != 0);
+            } else {
+                // o = Fc V into [0,128), as the output kernel forms it: the
+                // 64-row Fc image as a 128-row operand (its rows 64-127, the
+                // next 8 KB, land in lanes that are not read)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_f16(s->tmem_base, make_desc(sbase + kOffStFc + kk * 32, 16, 1024, kSw128),
+                            make_desc(sbase + kOffStV + kk * 1024, 4096, 512, kSw64), idesc_b, kk != 0);
+            }
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
                 mma_f16(s->tmem_base + 128, make_desc(sbase + kOffStEc + kk * 32, 16, 1024, kSw128),
@@ -600,7 +633,7 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
     }
     // the R warps (q >= 2: warps 2, 3, 6, 7) turn R into Qc under the products
     // (q from the tile still in shared memory) and copy it out
-    if (q >= 2) {
+    if (q >= 2 && !single) {
         const float qs = s->gam[i] * s->rq[i];
 #pragma unroll
         for (int g = 0; g < 2; ++g)
@@ -624,6 +657,82 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
     }
     wait_bar(s, &s->mbar_mma, 1, p.status);
     tc_fence_after();
+    if (single) {
+        // final state row = lane (dk), value columns 64 ch ..: Bc through fp16,
+        // as the scan adds it to a zero state
+        float* fs = p.final_state + (((size_t)seq * hv + h) * kD + row) * kD + 64 * ch;
+        {
+            float bv[2][32];
+            tmem_ld32x2(s->tmem_base + ((uint32_t)(32 * q) << 16) + 128 + ch * 64,
+                        s->tmem_base + ((uint32_t)(32 * q) << 16) + 128 + ch * 64 + 32, bv[0], bv[1]);
+#pragma unroll
+            for (int g = 0; g < 2; ++g)
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4 *>(fs + 32 * g + e) =
+                        make_float4(__half2float(__float2half_rn(bv[g][e])), __half2float(__float2half_rn(bv[g][e + 1])),
+                                    __half2float(__float2half_rn(bv[g][e + 2])), __half2float(__float2half_rn(bv[g][e + 3])));
+        }
+        // outputs: token row = lane of quadrants 0-1 (warps 0, 1, 4, 5), value
+        // columns 64 ch .. as two 32-column quarters, with the output kernel's
+        // arithmetic: scale, the row's sum of squares over the four quarters
+        // in order, gated RMSNorm, bf16 of the valid rows
+        if (q < 2) {
+            constexpr float kScale = 0.088388347648318440550f;   // 1/sqrt(128)
+            float *red = reinterpret_cast<float *>(sm + kOffBM);   // [quarter][row]: BM is not used here
+            const uint32_t ta = s->tmem_base + ((uint32_t)(32 * q) << 16) + 64 * ch;
+            const bool norm = p.z != nullptr;
+            const __nv_bfloat16 *zp = norm ? reinterpret_cast<const __nv_bfloat16 *>(p.z)
+                                             + (int64_t)(tok0 + row) * p.in.z.t + (int64_t)h * p.in.z.h + 64 * ch
+                                           : nullptr;
+            float rn = 1.f;
+            if (norm) {
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    float o[32];
+                    tmem_ld32(ta + 32 * g, o);
+                    float ss = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        o[e] *= kScale;
+                        ss = fmaf(o[e], o[e], ss);
+                    }
+                    red[(2 * ch + g) * 64 + row] = ss;
+                }
+                named_sync(2, 128);   // warps 0, 1, 4, 5
+                rn = rsqrtf((red[row] + red[64 + row] + red[128 + row] + red[192 + row]) * (1.f / kD) + p.eps);
+            }
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                float o[32];
+                tmem_ld32(ta + 32 * g, o);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] *= kScale;
+                if (norm) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        float zf[8], wf[8];
+                        unpack8(row < L ? reinterpret_cast<const uint4 *>(zp + 32 * g)[u] : make_uint4(0, 0, 0, 0), zf);
+                        unpack8(reinterpret_cast<const uint4 *>(p.norm_w)[8 * ch + 4 * g + u], wf);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)   // silu(z) = z / (1 + e^-z)
+                            o[8 * u + e] = o[8 * u + e] * rn * wf[e] * __fdividef(zf[e], 1.f + __expf(-zf[e]));
+                    }
+                }
+                if (row < L) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out)
+                                                           + ((size_t)(tok0 + row) * hv + h) * kD + 64 * ch + 32 * g);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        float v8[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v8[e] = o[8 * u + e];
+                        dst[u] = pack8(v8);
+                    }
+                }
+            }
+        }
+    } else {
     // Mc row = lane (output dk), columns = input dk half ch
     {
         float mv[2][32];
@@ -676,6 +785,8 @@ prep_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap tm_q, const __gri
             }
         }
     }
+
+    }   // the records of a call that continues in the scan and output kernels
 
     // ---- teardown: every record copy has completed before the CTA exits (each
     //      issuing lane waits for its own).  Waiting only for the copies to
@@ -808,7 +919,9 @@ cudaError_t launch_prefill_prep(const PrefillArgs &p, cudaStream_t stream)
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return cudaErrorInvalidDevice;
     if (!configured[dev].load(std::memory_order_relaxed)) {
-        cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess)
             return e;
         configured[dev].store(true, std::memory_order_relaxed);
@@ -819,7 +932,10 @@ cudaError_t launch_prefill_prep(const PrefillArgs &p, cudaStream_t stream)
         || !encode_tile_map(&tv, p.v, p.hv, p.total_tokens, p.in.v.t, p.in.v.h))
         return cudaErrorInvalidValue;
     dim3 grid(p.max_chunks, p.hv);
-    prep_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p, tq, tk, tv);
+    if (p.single_chunk)
+        prep_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(p, tq, tk, tv);
+    else
+        prep_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(p, tq, tk, tv);
     return cudaGetLastError();
 }
 

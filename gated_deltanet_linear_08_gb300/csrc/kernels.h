@@ -71,6 +71,7 @@ struct PrefillArgs {
     float *final_state;
     unsigned char *workspace;
     uint32_t *status;
+    int single_chunk;              // set by launch_prefill: prep finishes the call (see there)
 };
 
 // Workspace layout of the chunked prefill (all offsets 1024-byte aligned).
@@ -162,9 +163,17 @@ inline cudaError_t launch_prefill(const PrefillArgs &args, cudaStream_t stream)
         if (e != cudaSuccess)
             return e;
     }
+    // Every sequence within one chunk (64 tokens or fewer in all), a zero
+    // initial state and no conv: the state entering each chunk is zero, so
+    // prep computes the outputs and final states itself and the scan and
+    // output kernels do not run.
+    const bool single = args.total_tokens > 0 && args.total_tokens <= 64 && !args.init_state
+                        && args.conv.width == 0;
     if (args.total_tokens > 0) {
-        cudaError_t e = launch_prefill_prep(args, stream);
-        if (e != cudaSuccess)
+        PrefillArgs a = args;
+        a.single_chunk = single ? 1 : 0;
+        cudaError_t e = launch_prefill_prep(a, stream);
+        if (e != cudaSuccess || single)
             return e;
     }
     cudaError_t e = launch_prefill_scan(args, stream);

@@ -6,8 +6,8 @@ carried; 16 varlen sequences at Hv=48), the chunk boundaries the pegainfer
 page tests ("feat(qwen35): add SM120 FlashInfer GDN prefill candidate",
 Correctness: T = 1, 2, 63, 64, 65, 127, 128; chunked vs unchunked prefill),
 grouped heads, empty sequences, in-place state, weak and pure decay, long
-sequences (16,384 tokens; 8,192 with weak decay), and run-to-run
-determinism.
+sequences (16,384 tokens; 8,192 with weak decay), run-to-run determinism,
+and the single-chunk calls that prep finishes on its own.
 """
 import math
 
@@ -254,3 +254,33 @@ def test_prefill_more_chains_than_scan_ctas():
         ro, rs = oracle_prefill(sub)
         assert_out_close(go[s:e], ro, f"chains {first}-{last} out")
         assert_state_close(gs[first:last], rs, f"chains {first}-{last} state")
+
+
+@pytest.mark.parametrize("lens,gated", [([64], True), ([1], False), ([63], True), ([30, 0, 34], False),
+                                        ([3, 0, 0, 5, 1, 0, 7, 2, 0, 9, 4, 0, 6, 1, 0, 8, 3, 0, 2, 5], True)],
+                         ids=["T64_gnorm", "T1", "T63_gnorm", "three_one_empty", "twenty_with_index"])
+def test_prefill_single_chunk_call_equals_the_scan_path(lens, gated):
+    """A call of 64 tokens or fewer with no initial state is finished inside
+    prep (no scan or output kernel).  It equals the same call with an
+    explicit all-zero initial state, which runs every kernel, bit for bit
+    (outputs and final states, empty sequences included), and the oracle."""
+    import gated_deltanet_linear_08_gb300 as gdn
+    x = make_prefill_inputs(PrefillCase("single", seqlens=lens, hk=16, hv=32, gated_norm=gated, seed=41))
+    from parity_util import to_dev
+    d = to_dev(x)
+    N = len(lens)
+    args = (d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["cu_seqlens"])
+    kw = dict(z=d["z"], norm_w=d["norm_w"], eps=x["eps"])
+    o1, s1 = gdn.prefill(*args, **kw)
+    zero = torch.zeros(N, 32, 128, 128, dtype=torch.float32, device="cuda")
+    o2, s2 = gdn.prefill(*args, init_state=zero, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
+    assert torch.equal(s1, s2)
+    for n in range(N):
+        if lens[n] == 0:
+            assert int(torch.count_nonzero(s1[n])) == 0
+    assert gdn.check_device_status() == 0
+    ro, rs = oracle_prefill(x)
+    assert_out_close(o1.double().cpu().numpy(), ro, "single out")
+    assert_state_close(s1.double().cpu().numpy(), rs, "single state")
