@@ -55,6 +55,27 @@ def test_prefill_reads_inputs_from_a_packed_projection():
     assert gdn.check_device_status() == 0
 
 
+def test_single_chunk_prefill_reads_inputs_from_a_packed_projection():
+    """A call of at most 64 tokens with no initial state, which prep finishes
+    on its own (z read through the token and head strides), on packed
+    inputs equals the dense call and the full path."""
+    import gated_deltanet_linear_08_gb300 as gdn
+    x = make_prefill_inputs(PrefillCase("packed_single", seqlens=[40, 0, 21], hk=2, hv=6, gated_norm=True,
+                                        seed=35))
+    d = to_dev(x)
+    args = (d["A_log"], d["dt_bias"], d["cu_seqlens"])
+    ref_out, ref_fin = gdn.prefill(d["q"], d["k"], d["v"], d["a"], d["b"], *args, z=d["z"], norm_w=d["norm_w"],
+                                   eps=x["eps"])
+    buf, q, k, v, z, b, a = _pack(d["q"], d["k"], d["v"], d["z"], d["b"], d["a"])
+    out, fin = gdn.prefill(q, k, v, a, b, *args, z=z, norm_w=d["norm_w"], eps=x["eps"])
+    zero = torch.zeros_like(ref_fin)
+    full_out, full_fin = gdn.prefill(q, k, v, a, b, *args, init_state=zero, z=z, norm_w=d["norm_w"], eps=x["eps"])
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_out) and torch.equal(fin, ref_fin)
+    assert torch.equal(out, full_out) and torch.equal(fin, full_fin)
+    assert gdn.check_device_status() == 0
+
+
 def test_decode_reads_inputs_from_a_packed_projection():
     import gated_deltanet_linear_08_gb300 as gdn
     x = make_decode_slots_inputs(DecodeSlotsCase("packed_dec", batch=10, tokens=3, slots=16, skipped=1,
