@@ -73,11 +73,6 @@ __device__ __forceinline__ uint4 pack8h(const float (&v)[8])
 {
     return make_uint4(pack2h(v[0], v[1]), pack2h(v[2], v[3]), pack2h(v[4], v[5]), pack2h(v[6], v[7]));
 }
-__device__ __forceinline__ uint16_t bf16_bits(float x)
-{
-    __nv_bfloat16 h = __float2bfloat16_rn(x);
-    return *reinterpret_cast<uint16_t *>(&h);
-}
 __device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
 __device__ __forceinline__ void set_status(uint32_t *status, uint32_t bits)

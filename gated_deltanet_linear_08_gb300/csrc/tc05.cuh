@@ -22,13 +22,8 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// Byte offset of element (row, col) in a K-major 128B-swizzled tile whose rows
-// hold 64 bf16 (col < 64).
-__device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col)
-{
-    return row * 128u + ((((col >> 3) ^ row) & 7u) << 4) + ((col & 7u) << 1);
-}
-// Byte offset of 16-byte chunk `chunk` (0..7) of row `row`.
+// Byte offset of 16-byte chunk `chunk` (0..7) of row `row` in a K-major
+// 128B-swizzled tile whose rows hold 64 16-bit elements.
 __device__ __forceinline__ uint32_t sw128_chunk_offset(uint32_t row, uint32_t chunk)
 {
     return row * 128u + (((chunk ^ row) & 7u) << 4);
@@ -174,7 +169,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32])
         r[i] = __uint_as_float(u[i]);
 }
 
-// 16 consecutive fp32 columns of this thread's TMEM lane.
 // Two 32-column loads (addresses ta, tb) in flight together, one wait.
 __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float (&a)[32], float (&b)[32])
 {
@@ -204,21 +198,6 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float (&a)
         a[i] = __uint_as_float(u[i]);
         b[i] = __uint_as_float(v[i]);
     }
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&r)[16])
-{
-    uint32_t u[16];
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
-                 "tcgen05.wait::ld.sync.aligned;"
-                 : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]),
-                   "=r"(u[6]), "=r"(u[7]), "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]),
-                   "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
-                 : "r"(taddr) : "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        r[i] = __uint_as_float(u[i]);
 }
 
 // The sum of two 16-column TMEM loads (addresses ta, tb): both in flight
